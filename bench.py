@@ -1,0 +1,376 @@
+"""Benchmark: the 25-point (radius 4, 8th-order) Laplacian sweep, fp32, on a 512^3 grid.
+
+One step = one stencil_apply over the whole 512^3 grid (plan cached), inputs resident
+in HBM.  The grid (512 MiB in, 512 MiB out) is larger than L2, so no flush is needed
+between steps.  Also measured in the same run: the fused acoustic wave step on 640^3
+("wave" key), the end-to-end host-buffer call ("e2e"), SM clocks during the timed
+region, and the CPU oracle on the host cores ("cpu_baseline").
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun) runs independent replicas, one per GPU: the path has no
+exchange step at this size, so ranks never communicate on the data path; the value is
+the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from seismic_wave_propagation_gb300 import synth, traffic  # noqa: E402
+
+METRIC = "GPoints/s and achieved HBM GB/s (% of GB300 peak), 25-pt R=4 fp32 at 512^3"
+NX = NY = NZ = 512
+R = 4
+WAVE_N = 640
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "seismic_wave_propagation_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[key]
+        if e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist, rank, local, world
+    return None, 0, 0, 1
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def time_oracle(u: np.ndarray, c: np.ndarray, budget_s: float, min_reps: int = 1):
+    """Oracle sweeps over z-slabs of the grid until ~budget_s; returns (points/s, sample, cores)."""
+    import oracle
+    oracle.build()
+    nz = u.shape[0]
+    c32 = c.astype(np.float32)
+    # calibrate on a thin slab
+    slab = u[: 2 * R + 8]
+    t0 = time.perf_counter()
+    oracle.apply(slab, c32, R)
+    rate = traffic.interior_points(NX, NY, 2 * R + 8, R) / max(1e-9, time.perf_counter() - t0)
+    planes = int(max(1, min(nz - 2 * R, rate * budget_s / ((NX - 2 * R) * (NY - 2 * R)))))
+    sub = np.ascontiguousarray(u[: planes + 2 * R])
+    pts = traffic.interior_points(NX, NY, planes + 2 * R, R)
+    reps, t = 0, 0.0
+    out = sub.copy()
+    while reps < min_reps or t < budget_s * 0.5:
+        t0 = time.perf_counter()
+        oracle.apply(sub, c32, R, out=out)
+        t += time.perf_counter() - t0
+        reps += 1
+        if t > budget_s:
+            break
+    sample = f"{reps} oracle sweep(s) of a {NX}x{NY}x{planes + 2 * R} slab of the 512^3 grid ({pts} interior points each)"
+    return pts * reps / t, sample, oracle.num_threads()
+
+
+def run_reference(args, dist, rank, world):
+    """Reference arm: the CPU oracle as it stands, on the host cores, same metric/config."""
+    if rank != 0:
+        return
+    c = synth.laplacian8_coeffs()
+    u = synth.uniform_field(NX, NY, NZ)
+    import oracle
+    oracle.build()
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(u, c, per_step)
+    vals, samples = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, sample, cores = time_oracle(u, c, per_step)
+        vals.append(v)
+        samples.append(sample)
+    wall = time.perf_counter() - t0
+    gpts = statistics.median(vals) / 1e9
+    line = {"metric": METRIC, "impl": "reference", "value": gpts, "unit": "GPoints/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "star25_lap8_512", "nx": NX, "ny": NY, "nz": NZ, "radius": R,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": gpts, "unit": "GPoints/s", "cores": cores, "kind": "oracle",
+                             "sample": samples[-1] if samples else ""},
+            "e2e": {"value": gpts, "unit": "GPoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, dist, rank, local, world):
+    import torch
+    from seismic_wave_propagation_gb300 import StencilPlan
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    peak, peak_kind = peaks()
+    c = synth.laplacian8_coeffs()
+
+    # ---- headline: 25-point sweep at 512^3 ---------------------------------------
+    u = synth.uniform_field(NX, NY, NZ)
+    d_in = torch.from_numpy(u.ravel()).to(dev)
+    d_out = d_in.clone()
+    plan = StencilPlan(NX, NY, NZ, R, c)
+    info = plan.launch_info(0)
+    s = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            plan.apply(d_in.data_ptr(), d_out.data_ptr(), s)
+        plan.status(s)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gpu_uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+        gpu_id = f"GPU-{gpu_uuid}" if gpu_uuid is not None and not str(gpu_uuid).startswith("GPU-") else (
+            str(gpu_uuid) if gpu_uuid is not None else None)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_id) as clk:
+            time.sleep(0.25)
+            whole0.record(stream)
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                plan.apply(d_in.data_ptr(), d_out.data_ptr(), s)
+                ev[i][1].record(stream)
+            whole1.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier(dist)
+        plan.status(s)
+    total_ms = whole0.elapsed_time(whole1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    total_ms = max_over_ranks(dist, total_ms)
+    interior = traffic.interior_points(NX, NY, NZ, R)
+    pts_all = sum_over_ranks(dist, float(interior * args.steps))
+    gpts = pts_all / (total_ms / 1e3) / 1e9
+    algo_bytes = traffic.apply_bytes(NX, NY, NZ, R)
+    achieved = algo_bytes / avg_launch_s / 1e9
+    clocks = clk.summary()
+
+    # ---- fused wave step at 640^3 ----------------------------------------------------
+    del d_out
+    wave = None
+    if not args.skip_wave:
+        n = WAVE_N
+        up, uu, vv, ee = synth.wave_fields(n, n, n)
+        f = [torch.from_numpy(a.ravel()).to(dev) for a in (up, uu, vv, ee)]
+        nxt = f[0].clone()
+        wplan = StencilPlan(n, n, n, R, c)
+        a, b = f[0], f[1]
+        wsteps = max(10, min(200, args.steps // 20))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                wplan.wave_step(a.data_ptr(), b.data_ptr(), nxt.data_ptr(), f[2].data_ptr(), f[3].data_ptr(), s)
+                a, b, nxt = b, nxt, a
+            wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(wsteps)]
+            torch.cuda.synchronize(dev)
+            for i in range(wsteps):
+                wev[i][0].record(stream)
+                wplan.wave_step(a.data_ptr(), b.data_ptr(), nxt.data_ptr(), f[2].data_ptr(), f[3].data_ptr(), s)
+                wev[i][1].record(stream)
+                a, b, nxt = b, nxt, a
+            torch.cuda.synchronize(dev)
+            wplan.status(s)
+        wms = statistics.mean([x.elapsed_time(y) for x, y in wev])
+        wbytes = traffic.wave_bytes(n, n, n, R)
+        wint = traffic.interior_points(n, n, n, R)
+        wave = {"workload": "wave25_640", "steps": wsteps, "ms_per_step": wms,
+                "gpoints_per_s": wint / (wms / 1e3) / 1e9,
+                "roofline": {"bound": "hbm", "achieved": wbytes / (wms / 1e3) / 1e9, "peak": peak,
+                             "unit": "GB/s", "frac": wbytes / (wms / 1e3) / 1e9 / peak,
+                             "traffic": profiled_traffic("wave25_640")},
+                "launch": wplan.launch_info(1)}
+        wplan.close()
+        del f, nxt, a, b
+
+    # ---- end to end through the host-buffer C-ABI call --------------------------------
+    h_in = torch.from_numpy(u.ravel()).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    in_np, out_np = h_in.numpy(), h_out.numpy()
+    plan.apply_host(in_np, out_np, 1, s)
+    e2e_steps = max(3, min(20, args.steps // 100))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        plan.apply_host(in_np, out_np, 1, s)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = max_over_ranks(dist, e2e_s)
+    e2e = {"value": sum_over_ranks(dist, float(interior)) / e2e_s / 1e9, "unit": "GPoints/s",
+           "h2d_bytes_per_step": 4 * NX * NY * NZ, "d2h_bytes_per_step": 4 * NX * NY * NZ,
+           "ms_per_step": e2e_s * 1e3, "steps": e2e_steps}
+    plan.close()
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ---------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        v, sample, cores = time_oracle(u, c, args.cpu_budget)
+        cpu = {"value": v / 1e9, "unit": "GPoints/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": gpts, "unit": "GPoints/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": "star25_lap8_512", "nx": NX, "ny": NY, "nz": NZ, "radius": R,
+                           "coeffs": "8th-order Laplacian, h=1", "l2": "inputs (512 MiB) larger than L2; no flush",
+                           "parallelism": "replicas" if world > 1 else "single GPU",
+                           "launch": info},
+                "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": profiled_traffic("star25_512"),
+                             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                             else "fallback 6.8 TB/s",
+                             "algorithmic_bytes_per_launch": algo_bytes,
+                             "avg_launch_ms": avg_launch_s * 1e3},
+                "gpu_launches": args.steps,
+                "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                           "reasons": clocks["reasons"], "samples": clocks["samples"]},
+                "e2e": e2e, "cpu_baseline": cpu, "wave": wave}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-wave", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist, rank, local, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, dist, rank, world)
+    else:
+        from seismic_wave_propagation_gb300 import build as b
+        b.build()
+        run_ours(args, dist, rank, local, world)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

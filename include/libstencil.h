@@ -1,0 +1,144 @@
+/*
+ * libstencil: 3D star-stencil sweeps and the fused acoustic wave step on NVIDIA GB300.
+ *
+ * Problem statement followed by every entry point:
+ *  - Fields are flat 1D fp32 arrays with x innermost: point (x, y, z) lives at
+ *    i = x + nx*(y + ny*z) (64-bit arithmetic).  "Accelerating High-Order Stencils on
+ *    GPUs", 3D blocking with global memory: the grid is a flat 1D array and X, the
+ *    innermost dimension, is the coalescing axis.
+ *  - The star stencil of radius R computes, at every point at least R away from every
+ *    face,
+ *        out = coeffs[0]*u + sum_{r=1..R} coeffs[r] * (u at the six points at distance r
+ *                                                       along +-x, +-y, +-z).
+ *    coeffs[0] is the TOTAL centre weight (the three axes summed); coeffs[r] weighs each
+ *    of the six neighbours at distance r.  Same page (the 25-point stencil reads four
+ *    neighbours per direction per axis) and "Thread Coarsening 與 Register Tiling",
+ *    Fig 8.10 (seven-point case; boundary points are not written).
+ *  - Points closer than R to any face (the "shell") are NEVER written by any call.
+ *
+ * Memory ownership: the caller owns every field (device memory of the plan's device,
+ * allocated by any allocator, e.g. PyTorch).  A plan owns a small device status block,
+ * a cache of TMA descriptors and, only for the *_host entry points, a device workspace
+ * allocated on their first call.  A plan must not be used by two host threads at once.
+ *
+ * Asynchrony: stencil_apply and wave_step only enqueue work on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream) and return.  STENCIL_OK means "enqueued".  A device
+ * side failure (a bounded wait that ran out) is reported by stencil_plan_status.
+ *
+ * Errors: every int-returning call returns STENCIL_OK (0) or a negative code below;
+ * stencil_last_error() then holds a message for the calling host thread.
+ */
+#ifndef LIBSTENCIL_H
+#define LIBSTENCIL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define STENCIL_OK 0
+#define STENCIL_ERR_ARG (-1)       /* null pointer, bad radius/size/count, wrong device */
+#define STENCIL_ERR_ALIGNMENT (-2) /* pointer not 16-byte aligned, or nx not a multiple of 4 */
+#define STENCIL_ERR_ALIAS (-3)     /* forbidden overlap between an input and the output */
+#define STENCIL_ERR_CUDA (-4)      /* CUDA runtime or driver error (launch, copy, alloc) */
+#define STENCIL_ERR_TIMEOUT (-5)   /* a kernel's bounded wait ran out (from stencil_plan_status) */
+
+#define STENCIL_MAX_RADIUS 4
+
+typedef struct stencil_plan stencil_plan; /* opaque */
+
+/*
+ * Create a plan for an nx x ny x nz grid and a star stencil of the given radius.
+ *  nx, ny, nz  >= 1; nx must be a multiple of 4 (TMA row pitch is a multiple of 16 B).
+ *              A grid with any dimension < 2*radius+1 has an empty interior: valid,
+ *              and every sweep is then a no-op.
+ *  radius      in [1, STENCIL_MAX_RADIUS].
+ *  coeffs      radius+1 host floats (see the stencil definition above); copied.
+ * The plan binds to the CUDA device current at creation.  Returns NULL on failure
+ * (stencil_last_error() says why).
+ */
+stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius,
+                                  const float* coeffs);
+
+/* Release the plan and everything it owns.  NULL is a no-op.  Synchronises nothing:
+ * the caller must ensure no work that uses the plan is still running. */
+void stencil_plan_destroy(stencil_plan* plan);
+
+/*
+ * One stencil sweep: out = stencil(in) on the interior; the shell of `out` is untouched.
+ * Callers wanting the shell copied (a "fixed boundary") pre-copy `in` into `out` once;
+ * ping-pong sweeps that start from two copies of the same field keep it fixed.
+ *  in, out   device pointers to nx*ny*nz floats, 16-byte aligned, must not overlap.
+ * Errors: STENCIL_ERR_ARG, _ALIGNMENT, _ALIAS, _CUDA.
+ */
+int stencil_apply(stencil_plan* plan, const float* in, float* out, void* stream);
+
+/*
+ * One time step of the acoustic isotropic wave equation with a sponge layer, fused
+ * into a single pass (the stencil of the plan is the Laplacian, h = 1):
+ *   u_next = (2*u - (1 - eta)*u_prev + v2dt2 * lap(u)) / (1 + eta)
+ * on the interior; the shell of u_next is untouched.  "Accelerating High-Order Stencils
+ * on GPUs" names the acoustic isotropic model, its fields u and eta and the PML region;
+ * the update above is the second-order leapfrog with a pointwise damping term.
+ *  All six pointers: device, nx*ny*nz floats, 16-byte aligned.
+ *  u_next must not overlap u, v2dt2 or eta.  u_next == u_prev exactly is allowed (each
+ *  point reads u_prev only where it writes u_next), which permits two-buffer stepping;
+ *  any partial overlap is STENCIL_ERR_ALIAS.
+ * Errors: STENCIL_ERR_ARG, _ALIGNMENT, _ALIAS, _CUDA.
+ */
+int wave_step(stencil_plan* plan, const float* u_prev, const float* u, float* u_next,
+              const float* v2dt2, const float* eta, void* stream);
+
+/*
+ * Synchronise `stream`, then report device-side failures of this plan's kernels since
+ * the previous call: STENCIL_ERR_TIMEOUT if a kernel's bounded wait for staged data ran
+ * out (its outputs are then undefined), STENCIL_ERR_CUDA on a CUDA error, else STENCIL_OK.
+ * Reading the status clears it.
+ */
+int stencil_plan_status(stencil_plan* plan, void* stream);
+
+/* Message describing the last error of the calling host thread ("" if none). */
+const char* stencil_last_error(void);
+
+/*
+ * Host-buffer convenience entry points.  They copy host arrays to a device workspace
+ * owned by the plan (allocated on first use, 2 or 4 fields), run on `stream`, copy the
+ * result back and synchronise the stream.  Host memory may be pageable or pinned
+ * (pinned overlaps better).  Return STENCIL_OK or an error code; a device timeout is
+ * reported as STENCIL_ERR_TIMEOUT.
+ *
+ * stencil_apply_host: out_host = `nsweeps` ping-pong sweeps of in_host with a fixed
+ *   shell (the shell of out_host equals that of in_host).  nsweeps >= 0.
+ * wave_run_host: `nsteps` wave steps from (u_prev_host, u_host); on return
+ *   u_prev_host and u_host hold the last two time levels (u_host the newest).
+ */
+int stencil_apply_host(stencil_plan* plan, const float* in_host, float* out_host,
+                       int nsweeps, void* stream);
+int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
+                  const float* v2dt2_host, const float* eta_host, int nsteps, void* stream);
+
+/*
+ * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step), written
+ * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
+ * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
+ * Returns the number of values written, or a negative error code.
+ */
+int stencil_plan_launch_info(const stencil_plan* plan, int kind, int64_t* info, int n);
+
+/*
+ * Test hook for the device watchdog: mode 1 makes every CTA of the plan's next launches
+ * skip one of its staged loads, so the bounded wait for it runs out and
+ * stencil_plan_status returns STENCIL_ERR_TIMEOUT; mode 0 restores normal operation.
+ * The wait limit is about two seconds.  Returns STENCIL_OK or STENCIL_ERR_ARG.
+ */
+int stencil_debug_inject(stencil_plan* plan, int mode);
+
+/* Library version string. */
+const char* stencil_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSTENCIL_H */

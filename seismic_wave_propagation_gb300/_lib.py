@@ -1,0 +1,183 @@
+"""ctypes binding of libstencil.so: the same entry points, argument marshalling only.
+
+Every computation runs in the CUDA library.  Fields may be passed as CUDA tensors
+(float32, contiguous) or as raw device addresses (int); host-buffer calls take numpy
+float32 arrays.  If the library is missing this module raises at the first call: there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libstencil.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "libstencil.h")
+
+STENCIL_OK = 0
+ERRORS = {-1: "STENCIL_ERR_ARG", -2: "STENCIL_ERR_ALIGNMENT", -3: "STENCIL_ERR_ALIAS",
+          -4: "STENCIL_ERR_CUDA", -5: "STENCIL_ERR_TIMEOUT"}
+KIND_APPLY, KIND_WAVE = 0, 1
+LAUNCH_INFO_KEYS = ("grid", "threads", "smem", "ctas_per_sm", "tiles", "zchunks", "tile_x",
+                    "tile_y", "stages", "sms")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class StencilError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {message}")
+        self.code = code
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/libstencil.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text.split('extern "C" {', 1)[1])
+
+
+def load():
+    """Load libstencil.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libstencil.so not built ({LIB_PATH}); run "
+                               "python -m seismic_wave_propagation_gb300.build")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, fp = ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_float)
+        lib.stencil_plan_create.argtypes = [i64, i64, i64, ctypes.c_int, fp]
+        lib.stencil_plan_create.restype = vp
+        lib.stencil_plan_destroy.argtypes = [vp]
+        lib.stencil_plan_destroy.restype = None
+        lib.stencil_apply.argtypes = [vp, vp, vp, vp]
+        lib.wave_step.argtypes = [vp] * 7
+        lib.stencil_plan_status.argtypes = [vp, vp]
+        lib.stencil_last_error.restype = ctypes.c_char_p
+        lib.stencil_apply_host.argtypes = [vp, vp, vp, ctypes.c_int, vp]
+        lib.wave_run_host.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
+        lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
+        lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
+        lib.stencil_version.restype = ctypes.c_char_p
+        for fn in ("stencil_apply", "wave_step", "stencil_plan_status", "stencil_apply_host",
+                   "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject"):
+            getattr(lib, fn).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().stencil_last_error().decode()
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise StencilError(rc, last_error())
+    return rc
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if x.dtype.__repr__() != "torch.float32" or not x.is_contiguous() or not x.is_cuda:
+            raise ValueError("fields must be contiguous float32 CUDA tensors")
+        return x.data_ptr()
+    raise TypeError(f"cannot take a device address of {type(x)}")
+
+
+def _stream(stream, *fields) -> int | None:
+    if stream is None:
+        for f in fields:
+            if hasattr(f, "is_cuda") and f.is_cuda:
+                import torch
+                return torch.cuda.current_stream(f.device).cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _host(a: np.ndarray, n: int) -> int:
+    if a.dtype != np.float32 or not a.flags.c_contiguous or a.size != n:
+        raise ValueError("host fields must be C-contiguous float32 arrays of nx*ny*nz values")
+    return a.ctypes.data
+
+
+class StencilPlan:
+    """A star stencil of ``radius`` on an nx x ny x nz grid (see include/libstencil.h)."""
+
+    def __init__(self, nx: int, ny: int, nz: int, radius: int, coeffs):
+        lib = load()
+        c = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32))
+        if c.ndim != 1:
+            raise ValueError("coeffs must be 1D")
+        self.nx, self.ny, self.nz, self.radius = int(nx), int(ny), int(nz), int(radius)
+        self.coeffs = c.copy()
+        self._p = lib.stencil_plan_create(self.nx, self.ny, self.nz, self.radius,
+                                          c.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+        if not self._p:
+            raise StencilError(-1, last_error())
+        self._lib = lib
+
+    @property
+    def npoints(self) -> int:
+        return self.nx * self.ny * self.nz
+
+    def close(self):
+        if getattr(self, "_p", None):
+            self._lib.stencil_plan_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def apply(self, inp, out, stream=None) -> None:
+        _check(self._lib.stencil_apply(self._p, _addr(inp), _addr(out), _stream(stream, inp, out)))
+
+    def wave_step(self, u_prev, u, u_next, v2dt2, eta, stream=None) -> None:
+        fields = (u_prev, u, u_next, v2dt2, eta)
+        _check(self._lib.wave_step(self._p, *[_addr(f) for f in fields], _stream(stream, *fields)))
+
+    def status(self, stream=None, *fields) -> None:
+        _check(self._lib.stencil_plan_status(self._p, _stream(stream, *fields)))
+
+    def apply_host(self, inp: np.ndarray, out: np.ndarray, nsweeps: int = 1, stream=None) -> None:
+        n = self.npoints
+        _check(self._lib.stencil_apply_host(self._p, _host(inp, n), _host(out, n), int(nsweeps),
+                                            _stream(stream)))
+
+    def wave_run_host(self, u_prev: np.ndarray, u: np.ndarray, v2dt2: np.ndarray, eta: np.ndarray,
+                      nsteps: int, stream=None) -> None:
+        n = self.npoints
+        _check(self._lib.wave_run_host(self._p, _host(u_prev, n), _host(u, n), _host(v2dt2, n),
+                                       _host(eta, n), int(nsteps), _stream(stream)))
+
+    def launch_info(self, kind: int = KIND_APPLY) -> dict:
+        buf = (ctypes.c_int64 * len(LAUNCH_INFO_KEYS))()
+        m = _check(self._lib.stencil_plan_launch_info(self._p, kind, buf, len(buf)))
+        return {k: int(buf[i]) for i, k in enumerate(LAUNCH_INFO_KEYS[:m])}
+
+    def debug_inject(self, mode: int) -> None:
+        _check(self._lib.stencil_debug_inject(self._p, int(mode)))
+
+
+def version() -> str:
+    return load().stencil_version().decode()

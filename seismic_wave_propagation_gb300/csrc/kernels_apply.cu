@@ -1,0 +1,17 @@
+// Stencil-sweep kernel instantiations, radius 1..4.
+// Tile 64 x 32 outputs, 256 threads (4 x 2 outputs per thread), ring of R+4 planes
+// (three planes in flight beyond the lead plane).
+#include "kernel_table.h"
+
+namespace libstencil {
+
+KernelDesc apply_kernel_desc(int radius) {
+  switch (radius) {
+    case 1: return make_desc<1, 2, 16, 5, 1, false, 1>();
+    case 2: return make_desc<2, 2, 16, 6, 1, false, 1>();
+    case 3: return make_desc<3, 2, 16, 7, 1, false, 1>();
+    default: return make_desc<4, 2, 16, 8, 1, false, 1>();
+  }
+}
+
+}  // namespace libstencil

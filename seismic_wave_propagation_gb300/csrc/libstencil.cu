@@ -1,0 +1,419 @@
+// libstencil C ABI: plans, argument validation, TMA descriptors, launch geometry,
+// device status, and the host-buffer convenience calls.  The declarations and their
+// contracts are in include/libstencil.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/libstencil.h"
+#include "kernel_table.h"
+
+using namespace libstencil;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(STENCIL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapEntry {
+  const void* ptr = nullptr;
+  int box_w = 0, box_h = 0;
+  uint64_t stamp = 0;
+  CUtensorMap map;
+};
+
+constexpr int kMapCache = 16;
+
+}  // namespace
+
+struct stencil_plan {
+  int64_t nx, ny, nz;
+  int radius;
+  float c[STENCIL_MAX_RADIUS + 1];
+  int device;
+  int num_sms;
+  KernelDesc kd[2];    // [0] apply, [1] wave
+  int occupancy[2];    // CTAs per SM
+  StarParams params[2];
+  int grid[2];
+  unsigned* d_status;  // 4 words
+  MapEntry maps[kMapCache];
+  uint64_t clock;
+  float* work;         // host-API workspace
+  size_t work_floats;
+  int debug_mode;
+};
+
+namespace {
+
+int64_t npoints(const stencil_plan* p) { return p->nx * p->ny * p->nz; }
+
+bool interior_empty(const stencil_plan* p) {
+  const int64_t m = 2 * (int64_t)p->radius + 1;
+  return p->nx < m || p->ny < m || p->nz < m;
+}
+
+// Choose the number of z-chunks per tile column: minimise the per-CTA step count of the
+// round-robin schedule (a filling step costs about a third of a computing one).
+void plan_geometry(stencil_plan* p, int kind) {
+  const KernelDesc& kd = p->kd[kind];
+  StarParams& sp = p->params[kind];
+  const int R = p->radius;
+  std::memset(&sp, 0, sizeof sp);
+  sp.nx = (int)p->nx;
+  sp.ny = (int)p->ny;
+  sp.nz = (int)p->nz;
+  for (int r = 0; r <= 4; ++r) sp.c[r] = r <= R ? p->c[r] : 0.0f;
+  sp.status = p->d_status;
+  sp.debug_skip = -1;
+  if (interior_empty(p)) {
+    p->grid[kind] = 0;
+    return;
+  }
+  sp.ntx = (int)((p->nx + kTX - 1) / kTX);
+  const int nty = (int)((p->ny - 2 * R + kd.tile_y - 1) / kd.tile_y);
+  sp.ntiles = sp.ntx * nty;
+  sp.nzi = (int)(p->nz - 2 * R);
+  const int64_t slots = (int64_t)p->num_sms * std::max(1, p->occupancy[kind]);
+  double best = 1e300;
+  int best_n = 1;
+  for (int n = 1; n <= sp.nzi; ++n) {
+    const int64_t items = (int64_t)sp.ntiles * n;
+    if (items > (int64_t)1 << 30) break;
+    const int64_t g = std::min<int64_t>(items, slots);
+    const int64_t rounds = (items + g - 1) / g;
+    const double steps = (double)((sp.nzi + n - 1) / n) + 0.35 * 2 * R;
+    const double cost = (double)rounds * steps;
+    if (cost < best * (1.0 - 1e-9)) {
+      best = cost;
+      best_n = n;
+    }
+  }
+  sp.nchunks = best_n;
+  sp.nitems = sp.ntiles * best_n;
+  p->grid[kind] = (int)std::min<int64_t>(sp.nitems, slots);
+}
+
+int check_device(const stencil_plan* p) {
+  int d = -1;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (d != p->device)
+    return fail(STENCIL_ERR_ARG, "current device %d is not the plan's device %d", d, p->device);
+  return STENCIL_OK;
+}
+
+int check_field(const stencil_plan* p, const void* ptr, const char* name) {
+  if (!ptr) return fail(STENCIL_ERR_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(ptr) & 15u)
+    return fail(STENCIL_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(STENCIL_ERR_ARG, "%s is not a CUDA pointer (%s)", name, cudaGetErrorString(e));
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(STENCIL_ERR_ARG, "%s is not device memory", name);
+  if (a.device != p->device)
+    return fail(STENCIL_ERR_ARG, "%s lives on device %d, the plan on device %d", name, a.device,
+                p->device);
+  return STENCIL_OK;
+}
+
+bool overlap(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+// TMA descriptor for a field pointer and box shape (cached per plan).
+int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtensorMap** out) {
+  MapEntry* victim = &p->maps[0];
+  for (MapEntry& m : p->maps) {
+    if (m.ptr == ptr && m.box_w == box_w && m.box_h == box_h) {
+      m.stamp = ++p->clock;
+      *out = &m.map;
+      return STENCIL_OK;
+    }
+    if (m.stamp < victim->stamp) victim = &m;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail(STENCIL_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {(cuuint64_t)p->nx, (cuuint64_t)p->ny, (cuuint64_t)p->nz};
+  const cuuint64_t strides[2] = {(cuuint64_t)p->nx * 4, (cuuint64_t)(p->nx * p->ny) * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    victim->ptr = nullptr;
+    victim->stamp = 0;
+    return fail(STENCIL_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  }
+  victim->ptr = ptr;
+  victim->box_w = box_w;
+  victim->box_h = box_h;
+  victim->stamp = ++p->clock;
+  *out = &victim->map;
+  return STENCIL_OK;
+}
+
+int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
+           const float* eta, float* out, cudaStream_t stream) {
+  if (p->grid[kind] == 0) return STENCIL_OK;  // empty interior: nothing to do
+  const KernelDesc& kd = p->kd[kind];
+  const CUtensorMap *mu, *mp = nullptr, *mv = nullptr, *me = nullptr;
+  int rc = get_map(p, u, kd.box_w, kd.box_h, &mu);
+  if (rc) return rc;
+  if (kind == 1) {
+    if ((rc = get_map(p, uprev, kTX, kd.tile_y, &mp))) return rc;
+    if ((rc = get_map(p, v2dt2, kTX, kd.tile_y, &mv))) return rc;
+    if ((rc = get_map(p, eta, kTX, kd.tile_y, &me))) return rc;
+  } else {
+    mp = mv = me = mu;
+  }
+  StarParams sp = p->params[kind];
+  sp.out = out;
+  sp.debug_skip = p->debug_mode == 1 ? 2 * p->radius + 1 : -1;
+  // Copy the descriptors: the cache may evict entries while the launch is pending.
+  const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me;
+  cudaError_t e = kd.launch(dim3(p->grid[kind]), stream, a, b, c, d, sp);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return STENCIL_OK;
+}
+
+int ensure_work(stencil_plan* p, size_t floats) {
+  if (p->work_floats >= floats) return STENCIL_OK;
+  if (p->work) cudaFree(p->work);
+  p->work = nullptr;
+  p->work_floats = 0;
+  cudaError_t e = cudaMalloc(&p->work, floats * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+  p->work_floats = floats;
+  return STENCIL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* stencil_last_error(void) { return g_err; }
+
+const char* stencil_version(void) { return "libstencil 0.1 (sm_103a)"; }
+
+stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius,
+                                  const float* coeffs) {
+  g_err[0] = 0;
+  if (radius < 1 || radius > STENCIL_MAX_RADIUS) {
+    fail(STENCIL_ERR_ARG, "radius %d outside [1, %d]", radius, STENCIL_MAX_RADIUS);
+    return nullptr;
+  }
+  if (!coeffs) {
+    fail(STENCIL_ERR_ARG, "coeffs is NULL");
+    return nullptr;
+  }
+  if (nx < 1 || ny < 1 || nz < 1 || nx > (1 << 30) || ny > (1 << 30) || nz > (1 << 30) ||
+      nx * ny > ((int64_t)1 << 40) || nx * ny * nz > ((int64_t)1 << 40)) {
+    fail(STENCIL_ERR_ARG, "grid %lld x %lld x %lld out of range", (long long)nx, (long long)ny,
+         (long long)nz);
+    return nullptr;
+  }
+  if (nx % 4) {
+    fail(STENCIL_ERR_ALIGNMENT, "nx = %lld is not a multiple of 4", (long long)nx);
+    return nullptr;
+  }
+  stencil_plan* p = new stencil_plan();
+  p->nx = nx;
+  p->ny = ny;
+  p->nz = nz;
+  p->radius = radius;
+  for (int r = 0; r <= STENCIL_MAX_RADIUS; ++r) p->c[r] = r <= radius ? coeffs[r] : 0.0f;
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e == cudaSuccess) e = cudaMalloc(&p->d_status, 4 * sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, 4 * sizeof(unsigned));
+  if (e != cudaSuccess) {
+    cuda_fail(e, "plan setup");
+    stencil_plan_destroy(p);
+    return nullptr;
+  }
+  p->kd[0] = apply_kernel_desc(radius);
+  p->kd[1] = wave_kernel_desc(radius);
+  for (int k = 0; k < 2; ++k) {
+    e = cudaFuncSetAttribute(p->kd[k].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->kd[k].smem);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p->occupancy[k], p->kd[k].fn,
+                                                        p->kd[k].threads, p->kd[k].smem);
+    if (e != cudaSuccess || p->occupancy[k] < 1) {
+      if (e == cudaSuccess) fail(STENCIL_ERR_CUDA, "kernel cannot be resident (occupancy 0)");
+      else cuda_fail(e, "kernel attributes");
+      stencil_plan_destroy(p);
+      return nullptr;
+    }
+    plan_geometry(p, k);
+  }
+  return p;
+}
+
+void stencil_plan_destroy(stencil_plan* p) {
+  if (!p) return;
+  if (p->d_status) cudaFree(p->d_status);
+  if (p->work) cudaFree(p->work);
+  delete p;
+}
+
+int stencil_apply(stencil_plan* p, const float* in, float* out, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, in, "in")) || (rc = check_field(p, out, "out"))) return rc;
+  if (overlap(in, out, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
+  return launch(p, 0, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
+}
+
+int wave_step(stencil_plan* p, const float* u_prev, const float* u, float* u_next,
+              const float* v2dt2, const float* eta, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, u_prev, "u_prev")) || (rc = check_field(p, u, "u")) ||
+      (rc = check_field(p, u_next, "u_next")) || (rc = check_field(p, v2dt2, "v2dt2")) ||
+      (rc = check_field(p, eta, "eta")))
+    return rc;
+  const size_t bytes = (size_t)npoints(p) * 4;
+  if (overlap(u_next, u, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps u");
+  if (overlap(u_next, v2dt2, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps v2dt2");
+  if (overlap(u_next, eta, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps eta");
+  if (u_next != u_prev && overlap(u_next, u_prev, bytes))
+    return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
+  return launch(p, 1, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_plan_status(stencil_plan* p, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  int rc = check_device(p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned h[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h, p->d_status, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status");
+  if (h[0] == 0) return STENCIL_OK;
+  e = cudaMemsetAsync(p->d_status, 0, sizeof h, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  if (h[0] & kStatusBadSmem) return fail(STENCIL_ERR_CUDA, "shared memory base misaligned");
+  return fail(STENCIL_ERR_TIMEOUT,
+              "device wait for staged data ran out (flags 0x%x, block %u, load %u)%s", h[0], h[1],
+              h[2], (h[0] & kStatusDrainTimeout) ? "; copies still pending at exit" : "");
+}
+
+int stencil_apply_host(stencil_plan* p, const float* in_host, float* out_host, int nsweeps,
+                       void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (!in_host || !out_host) return fail(STENCIL_ERR_ARG, "NULL host buffer");
+  if (nsweeps < 0) return fail(STENCIL_ERR_ARG, "nsweeps < 0");
+  int rc = check_device(p);
+  if (rc) return rc;
+  const size_t n = (size_t)npoints(p);
+  if ((rc = ensure_work(p, 2 * n))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->work;
+  float* b = p->work + n;
+  cudaError_t e = cudaMemcpyAsync(a, in_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && nsweeps > 0) e = cudaMemcpyAsync(b, a, n * 4, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copy in");
+  for (int i = 0; i < nsweeps; ++i) {
+    if ((rc = launch(p, 0, a, nullptr, nullptr, nullptr, b, s))) return rc;
+    std::swap(a, b);
+  }
+  e = cudaMemcpyAsync(out_host, a, n * 4, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copy out");
+  return stencil_plan_status(p, stream);
+}
+
+int wave_run_host(stencil_plan* p, float* u_prev_host, float* u_host, const float* v2dt2_host,
+                  const float* eta_host, int nsteps, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (!u_prev_host || !u_host || !v2dt2_host || !eta_host)
+    return fail(STENCIL_ERR_ARG, "NULL host buffer");
+  if (nsteps < 0) return fail(STENCIL_ERR_ARG, "nsteps < 0");
+  int rc = check_device(p);
+  if (rc) return rc;
+  const size_t n = (size_t)npoints(p);
+  if ((rc = ensure_work(p, 4 * n))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->work;  // u_prev, then overwritten by u_next (two-buffer stepping)
+  float* b = p->work + n;
+  float* v = p->work + 2 * n;
+  float* et = p->work + 3 * n;
+  cudaError_t e = cudaMemcpyAsync(a, u_prev_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b, u_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v, v2dt2_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(et, eta_host, n * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copy in");
+  for (int i = 0; i < nsteps; ++i) {
+    if ((rc = launch(p, 1, b, a, v, et, a, s))) return rc;
+    std::swap(a, b);
+  }
+  e = cudaMemcpyAsync(u_prev_host, a, n * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(u_host, b, n * 4, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copy out");
+  return stencil_plan_status(p, stream);
+}
+
+int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int n) {
+  if (!p || !info || n < 0 || kind < 0 || kind > 1) return fail(STENCIL_ERR_ARG, "bad arguments");
+  const KernelDesc& kd = p->kd[kind];
+  const StarParams& sp = p->params[kind];
+  const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.ntiles,
+                         sp.nchunks,    kTX,        kd.tile_y, kd.stages,       p->num_sms};
+  const int m = std::min(n, 10);
+  for (int i = 0; i < m; ++i) info[i] = v[i];
+  return m;
+}
+
+int stencil_debug_inject(stencil_plan* p, int mode) {
+  if (!p || mode < 0 || mode > 1) return fail(STENCIL_ERR_ARG, "bad arguments");
+  p->debug_mode = mode;
+  return STENCIL_OK;
+}
+
+}  // extern "C"

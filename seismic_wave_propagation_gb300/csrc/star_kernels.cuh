@@ -1,0 +1,462 @@
+// Star-stencil sweep kernels for sm_103a (GB300): 2.5D blocking with TMA staging.
+//
+// What is computed (radius R, fp32, flat grid with x innermost):
+//   out(x,y,z) = c0*u + sum_{r=1..R} c_r*(u(x±r,y,z) + u(x,y±r,z) + u(x,y,z±r))
+// at every point at least R away from every face; optionally fused with the acoustic
+// update u_next = (2u - (1-eta) u_prev + v2dt2*lap) / (1+eta).
+//
+// How ("Accelerating High-Order Stencils on GPUs", 2.5D blocking: a 2D x-y tile streams
+// through z; st_reg_fixed: the z column lives in 2R+1 per-thread registers and the loop is
+// unrolled 2R+1 times so that the window never moves):
+//   * One CTA owns a 64 x TY output tile of the x-y plane and a contiguous range of z
+//     (a "chunk").  Work items (tile, chunk) are dealt round-robin to a persistent grid in
+//     z-major order, so CTAs working on neighbouring tiles march through the same planes
+//     at the same time and their halos are served from L2.
+//   * Each plane's (64+8) x (TY+2R) box is staged into a shared-memory ring by TMA
+//     (cp.async.bulk.tensor.3d), one elected thread issuing, completion tracked by an
+//     mbarrier per slot (expect-tx bytes).  Out-of-range box parts are zero-filled by
+//     the TMA unit and only ever feed outputs that are masked off.
+//   * Every thread owns a 4 x TYT block of output columns (one float4 per row).  Its z
+//     window holds u at planes z-R..z+R for those columns: the lead plane z+R is read
+//     from the ring when it lands; in-plane neighbours of plane z come from the ring slot
+//     that plane z landed in R steps earlier; z neighbours come from the window.
+//   * Every wait on an mbarrier is bounded (about 2 s).  When it runs out the kernel
+//     records an error in the status block, waits (bounded) for its own copies still in
+//     flight and returns; the host reads the status.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace libstencil {
+
+constexpr int kTX = 64;             // output tile width in x (floats)
+constexpr int kThreadsX = kTX / 4;  // one float4 column group per thread
+constexpr int kHX = 4;              // staged x halo per side; keeps the TMA x start 16-B aligned
+
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusDrainTimeout = 2u;
+constexpr unsigned kStatusBadSmem = 4u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct StarParams {
+  int nx, ny, nz;
+  int ntx;          // tiles along x
+  int ntiles;       // tiles per plane
+  int nzi;          // interior planes (nz - 2R)
+  int nchunks;      // z chunks per tile column
+  int nitems;       // ntiles * nchunks
+  float c[5];       // c[0] total centre weight, c[r] per-neighbour weight
+  float* out;       // stencil output, or u_next for the wave step
+  unsigned* status; // [0] flags, [1] block, [2] load counter of the first failure
+  int debug_skip;   // load counter every CTA skips (watchdog test); -1 = none
+};
+
+// Producer cursor (kept in shared memory, touched by the elected thread only).
+struct Cursor {
+  int item, j, L, x0, y0, za, issued, pad;
+};
+
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE>
+struct StarCfg {
+  static constexpr int kThreads = kThreadsX * NWY;
+  static constexpr int TY = TYT * NWY;  // output tile height
+  static constexpr int BW = kTX + 2 * kHX;
+  static constexpr int BH = TY + 2 * R;
+  static constexpr int kPlaneBytes = BW * BH * 4;  // bytes one u box transfers
+  static constexpr int kPlaneStride = (kPlaneBytes + 127) / 128 * 128;
+  static constexpr int kAuxFieldBytes = kTX * TY * 4;
+  static constexpr int kAuxStageBytes = 3 * kAuxFieldBytes;
+  static constexpr int kNumBars = STAGES + (WAVE ? ASTAGES : 0);
+  static constexpr int kCurOff = (8 * kNumBars + 15) / 16 * 16;
+  static constexpr int kFlagOff = kCurOff + 2 * (int)sizeof(Cursor);
+  static constexpr int kRingOffset = (kFlagOff + 16 + 127) / 128 * 128;
+  static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
+  static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
+  static constexpr int kLookahead = STAGES - R - 1;  // planes in flight beyond the lead
+  static constexpr int NW = 2 * R + 1;               // z window depth
+  static_assert(kLookahead >= 1, "ring must hold planes z..z+R plus one in flight");
+  static_assert(BW <= 256 && BH <= 256, "TMA box dimensions are limited to 256");
+  static_assert((BW * 4) % 16 == 0, "TMA inner box bytes must be a multiple of 16");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+// ---- PTX wrappers ------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; false after ~kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it < (1u << 28); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) break;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+__device__ __forceinline__ float get(const float4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void set(float4& v, int e, float a) {
+  if (e == 0) v.x = a;
+  else if (e == 1) v.y = a;
+  else if (e == 2) v.z = a;
+  else v.w = a;
+}
+
+// ---- work decomposition -------------------------------------------------------------
+
+template <int R, int TY>
+__device__ __forceinline__ void item_geometry(const StarParams& p, int item, int& x0, int& y0,
+                                              int& za, int& zb) {
+  const int chunk = item / p.ntiles;
+  const int tile = item - chunk * p.ntiles;
+  const int by = tile / p.ntx;
+  const int bx = tile - by * p.ntx;
+  x0 = bx * kTX;
+  y0 = R + by * TY;
+  za = R + (int)(((long long)chunk * p.nzi) / p.nchunks);
+  zb = R + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
+}
+
+template <int R, int TY>
+__device__ __forceinline__ void cursor_set_item(const StarParams& p, Cursor& k, int item) {
+  k.item = item;
+  k.j = 0;
+  if (item < p.nitems) {
+    int x0, y0, za, zb;
+    item_geometry<R, TY>(p, item, x0, y0, za, zb);
+    k.x0 = x0;
+    k.y0 = y0;
+    k.za = za;
+    k.L = zb - za + 2 * R;
+  }
+}
+
+template <int R, int TY>
+__device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
+  if (++k.j == k.L) cursor_set_item<R, TY>(p, k, k.item + (int)gridDim.x);
+}
+
+// ---- the kernel ----------------------------------------------------------------------
+
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB>
+__global__ void __launch_bounds__(kThreadsX * NWY, MINB)
+    star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
+                      const __grid_constant__ CUtensorMap tm_uprev,
+                      const __grid_constant__ CUtensorMap tm_v2dt2,
+                      const __grid_constant__ CUtensorMap tm_eta, const StarParams p) {
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
+  constexpr int TY = C::TY;
+  constexpr int BW = C::BW;
+  constexpr int NW = C::NW;
+  constexpr int PSTRIDE = C::kPlaneStride / 4;  // floats between ring slots
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  Cursor* cur = reinterpret_cast<Cursor*>(smem + C::kCurOff);  // [0] u loads, [1] aux loads
+  const uint32_t base = smem_addr(smem);
+  const uint32_t ring_base = base + C::kRingOffset;
+  const uint32_t aux_base = base + C::kAuxOffset;
+  const float* ring = reinterpret_cast<const float*>(smem + C::kRingOffset);
+  const float* auxr = reinterpret_cast<const float*>(smem + C::kAuxOffset);
+
+  if ((int)blockIdx.x >= p.nitems) return;
+
+  const int tid = threadIdx.x;
+  const int col = 4 * (tid % kThreadsX);  // x offset of this thread's float4 in the tile
+  const int row0 = (tid / kThreadsX) * TYT;  // first tile row of this thread
+  const bool leader = tid == 0;
+
+  // Producer: stage the u box of the next plane in the cursor's sequence.
+  auto produce_u = [&](int counter) {
+    Cursor& k = cur[0];
+    if (k.item >= p.nitems) return;
+    const int slot = counter % STAGES;
+    const uint32_t bar = base + 8u * slot;
+    if (counter != p.debug_skip) {
+      mbar_arrive_expect_tx(bar, C::kPlaneBytes);
+      tma_load_3d(ring_base + slot * C::kPlaneStride, &tm_u, bar, k.x0 - kHX, k.y0 - R,
+                  k.za - R + k.j);
+    }
+    ++k.issued;
+    cursor_advance<R, TY>(p, k);
+  };
+  // Producer: stage u_prev, v2dt2, eta of the output plane of a computing step.
+  auto produce_aux = [&](int counter) {
+    Cursor& k = cur[1];
+    if (k.item >= p.nitems) return;
+    const int slot = counter % ASTAGES;
+    const uint32_t bar = base + 8u * (STAGES + slot);
+    if (k.j >= 2 * R) {
+      const uint32_t dst = aux_base + slot * C::kAuxStageBytes;
+      const int z = k.za + k.j - 2 * R;
+      mbar_arrive_expect_tx(bar, C::kAuxStageBytes);
+      tma_load_3d(dst, &tm_uprev, bar, k.x0, k.y0, z);
+      tma_load_3d(dst + C::kAuxFieldBytes, &tm_v2dt2, bar, k.x0, k.y0, z);
+      tma_load_3d(dst + 2 * C::kAuxFieldBytes, &tm_eta, bar, k.x0, k.y0, z);
+    } else {
+      mbar_arrive(bar);  // filling step: nothing to stage, just complete the phase
+    }
+    ++k.issued;
+    cursor_advance<R, TY>(p, k);
+  };
+
+  const bool bad_smem = (base & 127u) != 0u;  // TMA destinations need 128-B alignment
+  if (leader) {
+    if (bad_smem) atomicOr(p.status, kStatusBadSmem);
+    for (int s = 0; s < C::kNumBars; ++s) mbar_init(base + 8u * s, 1);
+    fence_mbar_init();
+    cursor_set_item<R, TY>(p, cur[0], blockIdx.x);
+    cur[0].issued = 0;
+    cur[1] = cur[0];
+  }
+  if (__syncthreads_or(bad_smem)) return;
+  if (leader) {
+    for (int c = 0; c <= C::kLookahead; ++c) produce_u(c);
+    if (WAVE)
+      for (int c = 0; c < ASTAGES; ++c) produce_aux(c);
+  }
+
+  bool failed = false;  // this thread saw a wait run out
+  auto fail = [&](int counter) {
+    if (atomicOr(p.status, kStatusTimeout) == 0u) {
+      p.status[1] = blockIdx.x;
+      p.status[2] = (unsigned)counter;
+    }
+    failed = true;
+  };
+  // Close a step: everyone is done with the slot of plane (lead - R); refill it.  The
+  // barrier also ORs the threads' failure flags, so the decision to stop is uniform.
+  auto end_step = [&](int J) -> bool {
+    const bool abort = __syncthreads_or(failed) != 0;
+    if (leader && !abort) {
+      fence_proxy_async_smem();
+      produce_u(J + STAGES - R);
+      if (WAVE) produce_aux(J + ASTAGES);
+    }
+    return abort;
+  };
+
+  float4 w[NW][TYT];  // z window: w[R] = plane z, w[2R] = lead plane z+R
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int k = 0; k < TYT; ++k) w[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  int J = 0;  // load counter of the current step
+  for (int item = blockIdx.x; item < p.nitems; item += gridDim.x) {
+    int x0, y0, za, zb;
+    item_geometry<R, TY>(p, item, x0, y0, za, zb);
+
+    // Fill: planes za-R .. za+R-1 enter the window; nothing to output yet.
+#pragma unroll
+    for (int f = 0; f < 2 * R; ++f) {
+      if (!mbar_wait_bounded(base + 8u * (J % STAGES), (J / STAGES) & 1)) fail(J);
+      const float* pl = ring + (J % STAGES) * PSTRIDE;
+#pragma unroll
+      for (int i = 0; i < NW - 1; ++i)
+#pragma unroll
+        for (int k = 0; k < TYT; ++k) w[i][k] = w[i + 1][k];
+#pragma unroll
+      for (int k = 0; k < TYT; ++k) w[NW - 1][k] = lds4(pl + (row0 + k + R) * BW + kHX + col);
+      const bool stop = end_step(J);
+      ++J;
+      if (stop) goto drain;
+    }
+
+    {
+      const int nout = zb - za;
+      const int gx = x0 + col;
+      for (int zo = 0;; zo += NW) {
+#pragma unroll
+        for (int s = 0; s < NW; ++s) {
+          if (zo + s >= nout) goto item_done;
+          const int z = za + zo + s;
+          if (!mbar_wait_bounded(base + 8u * (J % STAGES), (J / STAGES) & 1)) fail(J);
+          const float* pl = ring + (J % STAGES) * PSTRIDE;
+#pragma unroll
+          for (int i = 0; i < NW - 1; ++i)
+#pragma unroll
+            for (int k = 0; k < TYT; ++k) w[i][k] = w[i + 1][k];
+#pragma unroll
+          for (int k = 0; k < TYT; ++k) w[NW - 1][k] = lds4(pl + (row0 + k + R) * BW + kHX + col);
+
+          // Plane z sits in the slot it landed in R steps ago.
+          const float* pc = ring + ((J - R) % STAGES) * PSTRIDE;
+          float4 acc[TYT];
+#pragma unroll
+          for (int k = 0; k < TYT; ++k) {
+            const float4 cc = w[R][k];
+            const float* rowp = pc + (row0 + k + R) * BW + kHX + col;
+            float xs[4 + 2 * R];  // x = col-R .. col+3+R of this row
+            if constexpr (R >= 3) {
+              const float4 l = lds4(rowp - 4), r = lds4(rowp + 4);
+#pragma unroll
+              for (int e = 0; e < R; ++e) {
+                xs[R - 1 - e] = get(l, 3 - e);
+                xs[R + 4 + e] = get(r, e);
+              }
+            } else if constexpr (R == 2) {
+              const float2 l = *reinterpret_cast<const float2*>(rowp - 2);
+              const float2 r = *reinterpret_cast<const float2*>(rowp + 4);
+              xs[0] = l.x;
+              xs[1] = l.y;
+              xs[R + 4] = r.x;
+              xs[R + 5] = r.y;
+            } else {
+              xs[0] = rowp[-1];
+              xs[R + 4] = rowp[4];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) xs[R + e] = get(cc, e);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a = p.c[0] * xs[R + e];
+#pragma unroll
+              for (int r = 1; r <= R; ++r) {
+                const float s2 = (xs[R + e - r] + xs[R + e + r]) +
+                                 (get(w[R - r][k], e) + get(w[R + r][k], e));
+                a = fmaf(p.c[r], s2, a);
+              }
+              set(acc[k], e, a);
+            }
+          }
+          // y neighbours: every row within R of one of this thread's rows, each read once
+          // (rows of the thread itself come from the window).
+#pragma unroll
+          for (int h = -R; h < TYT + R; ++h) {
+            float4 v;
+            if (h >= 0 && h < TYT) v = w[R][h];
+            else v = lds4(pc + (row0 + h + R) * BW + kHX + col);
+#pragma unroll
+            for (int k = 0; k < TYT; ++k) {
+              const int d = h > k ? h - k : k - h;
+              if (d >= 1 && d <= R) {
+                acc[k].x = fmaf(p.c[d], v.x, acc[k].x);
+                acc[k].y = fmaf(p.c[d], v.y, acc[k].y);
+                acc[k].z = fmaf(p.c[d], v.z, acc[k].z);
+                acc[k].w = fmaf(p.c[d], v.w, acc[k].w);
+              }
+            }
+          }
+
+          if constexpr (WAVE) {
+            if (!mbar_wait_bounded(base + 8u * (STAGES + J % ASTAGES), (J / ASTAGES) & 1)) fail(J);
+            const float* pa = auxr + (J % ASTAGES) * (C::kAuxStageBytes / 4);
+#pragma unroll
+            for (int k = 0; k < TYT; ++k) {
+              const int o = (row0 + k) * kTX + col;
+              const float4 up = lds4(pa + o);
+              const float4 vv = lds4(pa + kTX * TY + o);
+              const float4 et = lds4(pa + 2 * kTX * TY + o);
+              const float4 uc = w[R][k];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float eta = get(et, e);
+                const float t = fmaf(get(vv, e), get(acc[k], e),
+                                     fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
+                set(acc[k], e, t / (1.0f + eta));
+              }
+            }
+          }
+
+#pragma unroll
+          for (int k = 0; k < TYT; ++k) {
+            const int gy = y0 + row0 + k;
+            if (gy < p.ny - R && gx < p.nx) {
+              float* dst = p.out + ((size_t)z * p.ny + gy) * p.nx + gx;
+              if (gx >= R && gx + 4 <= p.nx - R) {
+                __stcs(reinterpret_cast<float4*>(dst), acc[k]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (gx + e >= R && gx + e < p.nx - R) dst[e] = get(acc[k], e);
+              }
+            }
+          }
+
+          const bool stop = end_step(J);
+          ++J;
+          if (stop) goto drain;
+        }
+      }
+    }
+  item_done:;
+  }
+  return;
+
+drain:
+  // A wait ran out: make sure none of this CTA's copies is still landing in shared
+  // memory before the CTA exits (bounded as well), then leave.
+  if (leader) {
+    for (int c = J > 0 ? J - 1 : 0; c < cur[0].issued; ++c)
+      if (c != p.debug_skip && !mbar_wait_bounded(base + 8u * (c % STAGES), (c / STAGES) & 1))
+        atomicOr(p.status, kStatusDrainTimeout);
+    if (WAVE)
+      for (int c = J > 0 ? J - 1 : 0; c < cur[1].issued; ++c)
+        if (!mbar_wait_bounded(base + 8u * (STAGES + c % ASTAGES), (c / ASTAGES) & 1))
+          atomicOr(p.status, kStatusDrainTimeout);
+  }
+  __syncthreads();
+}
+
+}  // namespace libstencil

@@ -1,0 +1,129 @@
+"""Parity of the fused CUDA wave step against the CPU oracle (through the C ABI)."""
+import numpy as np
+import pytest
+
+import oracle
+from seismic_wave_propagation_gb300 import StencilPlan, synth
+from gpu_util import Guarded, interior_mask, sample_interior, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_wave(torch, up, u, s, e, c, R, nsteps, two_buffers=False):
+    nz, ny, nx = u.shape
+    plan = StencilPlan(nx, ny, nz, R, c)
+    d = [torch.from_numpy(np.ascontiguousarray(a).ravel()).cuda() for a in (up, u, s, e)]
+    a, b, sv, ev = d
+    nxt = a.clone()
+    for _ in range(nsteps):
+        if two_buffers:
+            plan.wave_step(a, b, a, sv, ev)
+            a, b = b, a
+        else:
+            plan.wave_step(a, b, nxt, sv, ev)
+            a, b, nxt = b, nxt, a
+    plan.status(None, a)
+    out = (a.cpu().numpy().reshape(u.shape), b.cpu().numpy().reshape(u.shape))
+    plan.close()
+    return out
+
+
+def rel_l2(x, y):
+    return float(np.linalg.norm((x.astype(np.float64) - y).ravel()) / np.linalg.norm(y.ravel().astype(np.float64)))
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4])
+def test_single_step_matches_oracle(R):
+    torch = torch_cuda()
+    nx, ny, nz = 136, 70, 40
+    c = np.random.default_rng(R).uniform(-0.3, 0.3, R + 1)
+    up = synth.uniform_field(nx, ny, nz, seed=7)
+    u = synth.uniform_field(nx, ny, nz, seed=8)
+    s = synth.uniform_field(nx, ny, nz, seed=9, scale=0.1) + np.float32(0.1)
+    e = synth.sponge_eta(nx, ny, nz, width=10)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    gs = [Guarded(torch, a) for a in (up, u, s, e)]
+    gn = Guarded(torch, u, fill_sentinel=True)
+    plan.wave_step(gs[0].ptr, gs[1].ptr, gn.ptr, gs[2].ptr, gs[3].ptr)
+    plan.status()
+    got = gn.numpy()
+    assert all(g.guards_intact() for g in gs + [gn])
+    want = oracle.wave_step(up, u, s, e, np.asarray(c, np.float32), R, u_next=np.zeros_like(u))
+    m = interior_mask(u.shape, R)
+    # one step: rounding of the stencil sum (scaled by v2dt2 <= 0.2) plus the update
+    tol = 1e-5 * (2 + 0.2 * float(np.sum(np.abs(c)))) * 2.0
+    assert np.max(np.abs(got[m] - want[m])) <= tol
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD)
+    plan.close()
+
+
+@pytest.mark.parametrize("two_buffers", [False, True])
+def test_multi_step_small(two_buffers):
+    torch = torch_cuda()
+    nx, ny, nz = 96, 80, 72
+    up, u, s, e = synth.wave_fields(nx, ny, nz)
+    c = synth.laplacian8_coeffs()
+    g_prev, g_cur = gpu_wave(torch, up, u, s, e, c, 4, 30, two_buffers)
+    o_prev, o_cur = oracle.run_wave(up, u, s, e, c.astype(np.float32), 4, 30)
+    assert rel_l2(g_cur, o_cur) <= 1e-5
+    assert rel_l2(g_prev, o_prev) <= 1e-5
+
+
+def test_sponge_absorbs_pulse_near_face():
+    """Pulse 6 points from a face on a 64^3 grid, 200 steps through the sponge."""
+    torch = torch_cuda()
+    n = 64
+    u = synth.gaussian_bump(n, n, n, sigma=3.0, center=(6, 32, 32))
+    s = synth.layered_v2dt2(n, n, n)
+    e = synth.sponge_eta(n, n, n)
+    c = synth.laplacian8_coeffs()
+    g_prev, g_cur = gpu_wave(torch, u.copy(), u, s, e, c, 4, 200)
+    o_prev, o_cur = oracle.run_wave(u.copy(), u, s, e, c.astype(np.float32), 4, 200)
+    assert rel_l2(g_cur, o_cur) <= 1e-4
+    assert np.all(np.isfinite(g_cur))
+
+
+def test_host_buffer_entry_matches_device_path():
+    torch = torch_cuda()
+    nx, ny, nz = 96, 40, 36
+    up, u, s, e = synth.wave_fields(nx, ny, nz)
+    c = synth.laplacian8_coeffs()
+    plan = StencilPlan(nx, ny, nz, 4, c)
+    hp, hu = up.copy(), u.copy()
+    plan.wave_run_host(hp, hu, s, e, 7)
+    g_prev, g_cur = gpu_wave(torch, up, u, s, e, c, 4, 7, two_buffers=True)
+    np.testing.assert_array_equal(hu, g_cur)
+    np.testing.assert_array_equal(hp, g_prev)
+    plan.close()
+
+
+def test_wave25_640_hundred_steps():
+    """The 640^3 acoustic run: 100 steps on the GPU and in the oracle from identical
+    inputs, relative L2 <= 1e-4; plus a per-step sampled check on the GPU's own state."""
+    torch = torch_cuda()
+    n = 640
+    up, u, s, e = synth.wave_fields(n, n, n)
+    c = synth.laplacian8_coeffs()
+    c32 = c.astype(np.float32)
+    plan = StencilPlan(n, n, n, 4, c)
+    d = [torch.from_numpy(a.ravel()).cuda() for a in (up, u, s, e)]
+    a, b, sv, ev = d
+    nxt = a.clone()
+    idx = sample_interior(u.shape, 4, 100000, planes=(320,))
+    for k in range(100):
+        if k in (0, 50):
+            hp, hc = a.cpu().numpy().reshape(u.shape), b.cpu().numpy().reshape(u.shape)
+        plan.wave_step(a, b, nxt, sv, ev)
+        if k in (0, 50):
+            plan.status(None, nxt)
+            want = oracle.wave_points(hp, hc, s, e, c32, 4, idx)
+            got = nxt.cpu().numpy()[idx]
+            assert np.max(np.abs(got - want)) <= 1e-5 * (2 + 0.2025 * 19.51) * float(np.max(np.abs(hc)))
+        a, b, nxt = b, nxt, a
+    plan.status(None, b)
+    g_cur = b.cpu().numpy().reshape(u.shape)
+    plan.close()
+    o_prev, o_cur = oracle.run_wave(up, u, s, e, c32, 4, 100)
+    r = rel_l2(g_cur, o_cur)
+    print(f"wave25 640^3 x100: relative L2 {r:.3e}, |u|_2 {np.linalg.norm(o_cur):.4f}")
+    assert r <= 1e-4
