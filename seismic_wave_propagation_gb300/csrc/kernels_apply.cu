@@ -1,6 +1,6 @@
 // Stencil-sweep kernel instantiations, radius 1..4.
-// Tile 64 x 32 outputs, 256 threads (4 x 2 outputs per thread), ring of R+4 planes
-// (three planes in flight beyond the lead plane).
+// Tile 64 x 32 outputs, 256 threads (4 x 2 outputs per thread).  Only the lead plane is
+// read from shared memory, so the ring is the landed plane plus R+3 (or 7) in flight.
 #include "kernel_table.h"
 
 namespace libstencil {

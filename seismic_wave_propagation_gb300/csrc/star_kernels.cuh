@@ -6,8 +6,7 @@
 // update u_next = (2u - (1-eta) u_prev + v2dt2*lap) / (1+eta).
 //
 // How ("Accelerating High-Order Stencils on GPUs", 2.5D blocking: a 2D x-y tile streams
-// through z; st_reg_fixed: the z column lives in 2R+1 per-thread registers and the loop is
-// unrolled 2R+1 times so that the window never moves):
+// through z, the z neighbours of a thread's points never leave its registers):
 //   * One CTA owns a 64 x TY output tile of the x-y plane and a contiguous range of z
 //     (a "chunk").  Work items (tile, chunk) are dealt round-robin to a persistent grid in
 //     z-major order, so CTAs working on neighbouring tiles march through the same planes
@@ -16,10 +15,15 @@
 //     (cp.async.bulk.tensor.3d), one elected thread issuing, completion tracked by an
 //     mbarrier per slot (expect-tx bytes).  Out-of-range box parts are zero-filled by
 //     the TMA unit and only ever feed outputs that are masked off.
-//   * Every thread owns a 4 x TYT block of output columns (one float4 per row).  Its z
-//     window holds u at planes z-R..z+R for those columns: the lead plane z+R is read
-//     from the ring when it lands; in-plane neighbours of plane z come from the ring slot
-//     that plane z landed in R steps earlier; z neighbours come from the window.
+//   * Every thread owns a 4 x TYT block of output columns (one float4 per row).  Along z
+//     it runs the symmetric 2R+1-tap filter h_i = c_|i-R| in transposed form: when plane
+//     p lands, its own values x update 2R running partial sums,
+//         y = h_0 x + s_1,   s_i <- h_i x + s_{i+1} (i < 2R),   s_2R <- h_2R x,
+//     and y is the z part of the output at plane p-R.  Each FMA also moves a partial sum
+//     one slot down, so the z window needs no register moves and no unrolling.  The
+//     in-plane part of plane p's outputs (x and y neighbours, read from the landed box)
+//     is added to s_R, which emerges R planes later.  The stencil sweep therefore needs
+//     only the lead plane in shared memory; the wave step keeps R more planes for u(z).
 //   * Every wait on an mbarrier is bounded (about 2 s).  When it runs out the kernel
 //     records an error in the status block, waits (bounded) for its own copies still in
 //     flight and returns; the host reads the status.
@@ -74,9 +78,9 @@ struct StarCfg {
   static constexpr int kRingOffset = (kFlagOff + 16 + 127) / 128 * 128;
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
   static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
-  static constexpr int kLookahead = STAGES - R - 1;  // planes in flight beyond the lead
-  static constexpr int NW = 2 * R + 1;               // z window depth
-  static_assert(kLookahead >= 1, "ring must hold planes z..z+R plus one in flight");
+  static constexpr int KEEP = WAVE ? R : 0;             // planes kept behind the lead
+  static constexpr int kLookahead = STAGES - KEEP - 1;  // planes in flight beyond the lead
+  static_assert(kLookahead >= 1, "ring must hold the kept planes plus one in flight");
   static_assert(BW <= 256 && BH <= 256, "TMA box dimensions are limited to 256");
   static_assert((BW * 4) % 16 == 0, "TMA inner box bytes must be a multiple of 16");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -152,6 +156,10 @@ __device__ __forceinline__ float4 lds4(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
+__device__ __forceinline__ float4 fma4(float a, const float4& x, const float4& y) {
+  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+
 __device__ __forceinline__ float get(const float4& v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
@@ -204,11 +212,11 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
                       const __grid_constant__ CUtensorMap tm_v2dt2,
-                      const __grid_constant__ CUtensorMap tm_eta, const StarParams p) {
+                      const __grid_constant__ CUtensorMap tm_eta, const __grid_constant__ StarParams p) {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
   constexpr int TY = C::TY;
   constexpr int BW = C::BW;
-  constexpr int NW = C::NW;
+  constexpr int KEEP = C::KEEP;
   constexpr int PSTRIDE = C::kPlaneStride / 4;  // floats between ring slots
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -222,8 +230,9 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   if ((int)blockIdx.x >= p.nitems) return;
 
   const int tid = threadIdx.x;
-  const int col = 4 * (tid % kThreadsX);  // x offset of this thread's float4 in the tile
+  const int col = 4 * (tid % kThreadsX);     // x offset of this thread's float4 in the tile
   const int row0 = (tid / kThreadsX) * TYT;  // first tile row of this thread
+  const int own = (row0 + R) * BW + kHX + col;  // its first point in a landed box
   const bool leader = tid == 0;
 
   // Producer: stage the u box of the next plane in the cursor's sequence.
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     ++k.issued;
     cursor_advance<R, TY>(p, k);
   };
-  // Producer: stage u_prev, v2dt2, eta of the output plane of a computing step.
+  // Producer: stage u_prev, v2dt2, eta of the output plane of an emitting step.
   auto produce_aux = [&](int counter) {
     Cursor& k = cur[1];
     if (k.item >= p.nitems) return;
@@ -284,163 +293,153 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     }
     failed = true;
   };
-  // Close a step: everyone is done with the slot of plane (lead - R); refill it.  The
-  // barrier also ORs the threads' failure flags, so the decision to stop is uniform.
-  auto end_step = [&](int J) -> bool {
-    const bool abort = __syncthreads_or(failed) != 0;
-    if (leader && !abort) {
-      fence_proxy_async_smem();
-      produce_u(J + STAGES - R);
-      if (WAVE) produce_aux(J + ASTAGES);
-    }
-    return abort;
-  };
 
-  float4 w[NW][TYT];  // z window: w[R] = plane z, w[2R] = lead plane z+R
+  // s[i][k]: partial sum of the output (i + 1 - R) planes after the current one, row k.
+  float4 s[2 * R][TYT];
 #pragma unroll
-  for (int i = 0; i < NW; ++i)
+  for (int i = 0; i < 2 * R; ++i)
 #pragma unroll
-    for (int k = 0; k < TYT; ++k) w[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < TYT; ++k) s[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  int J = 0;  // load counter of the current step
+  int J = 0;               // load counter of the current step
+  int slot = 0;            // J % STAGES
+  uint32_t phase = 0;      // (J / STAGES) & 1
+  int aslot = 0;           // J % ASTAGES
+  uint32_t aphase = 0;     // (J / ASTAGES) & 1
   for (int item = blockIdx.x; item < p.nitems; item += gridDim.x) {
     int x0, y0, za, zb;
     item_geometry<R, TY>(p, item, x0, y0, za, zb);
+    const int L = zb - za + 2 * R;  // planes za-R .. zb+R-1 land in turn
+    const int gx = x0 + col;
+    for (int j = 0; j < L; ++j) {
+      if (!mbar_wait_bounded(base + 8u * slot, phase)) fail(J);
+      const float* pl = ring + slot * PSTRIDE;
+      float4 xv[TYT];
+#pragma unroll
+      for (int k = 0; k < TYT; ++k) xv[k] = lds4(pl + own + k * BW);
 
-    // Fill: planes za-R .. za+R-1 enter the window; nothing to output yet.
+      if (j >= 2 * R) {
+        // Output plane z = (landed plane) - R is complete once its z part is added.
+        const int z = za + j - 2 * R;
+        float4 o[TYT];
 #pragma unroll
-    for (int f = 0; f < 2 * R; ++f) {
-      if (!mbar_wait_bounded(base + 8u * (J % STAGES), (J / STAGES) & 1)) fail(J);
-      const float* pl = ring + (J % STAGES) * PSTRIDE;
-#pragma unroll
-      for (int i = 0; i < NW - 1; ++i)
-#pragma unroll
-        for (int k = 0; k < TYT; ++k) w[i][k] = w[i + 1][k];
-#pragma unroll
-      for (int k = 0; k < TYT; ++k) w[NW - 1][k] = lds4(pl + (row0 + k + R) * BW + kHX + col);
-      const bool stop = end_step(J);
-      ++J;
-      if (stop) goto drain;
-    }
-
-    {
-      const int nout = zb - za;
-      const int gx = x0 + col;
-      for (int zo = 0;; zo += NW) {
-#pragma unroll
-        for (int s = 0; s < NW; ++s) {
-          if (zo + s >= nout) goto item_done;
-          const int z = za + zo + s;
-          if (!mbar_wait_bounded(base + 8u * (J % STAGES), (J / STAGES) & 1)) fail(J);
-          const float* pl = ring + (J % STAGES) * PSTRIDE;
-#pragma unroll
-          for (int i = 0; i < NW - 1; ++i)
-#pragma unroll
-            for (int k = 0; k < TYT; ++k) w[i][k] = w[i + 1][k];
-#pragma unroll
-          for (int k = 0; k < TYT; ++k) w[NW - 1][k] = lds4(pl + (row0 + k + R) * BW + kHX + col);
-
-          // Plane z sits in the slot it landed in R steps ago.
-          const float* pc = ring + ((J - R) % STAGES) * PSTRIDE;
-          float4 acc[TYT];
+        for (int k = 0; k < TYT; ++k) o[k] = fma4(p.c[R], xv[k], s[0][k]);
+        if constexpr (WAVE) {
+          if (!mbar_wait_bounded(base + 8u * (STAGES + aslot), aphase)) fail(J);
+          const float* pa = auxr + aslot * (C::kAuxStageBytes / 4);
+          int cs = slot - R;
+          if (cs < 0) cs += STAGES;
+          const float* pu = ring + cs * PSTRIDE + own;  // u at plane z (landed R steps ago)
 #pragma unroll
           for (int k = 0; k < TYT; ++k) {
-            const float4 cc = w[R][k];
-            const float* rowp = pc + (row0 + k + R) * BW + kHX + col;
-            float xs[4 + 2 * R];  // x = col-R .. col+3+R of this row
-            if constexpr (R >= 3) {
-              const float4 l = lds4(rowp - 4), r = lds4(rowp + 4);
-#pragma unroll
-              for (int e = 0; e < R; ++e) {
-                xs[R - 1 - e] = get(l, 3 - e);
-                xs[R + 4 + e] = get(r, e);
-              }
-            } else if constexpr (R == 2) {
-              const float2 l = *reinterpret_cast<const float2*>(rowp - 2);
-              const float2 r = *reinterpret_cast<const float2*>(rowp + 4);
-              xs[0] = l.x;
-              xs[1] = l.y;
-              xs[R + 4] = r.x;
-              xs[R + 5] = r.y;
-            } else {
-              xs[0] = rowp[-1];
-              xs[R + 4] = rowp[4];
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) xs[R + e] = get(cc, e);
+            const int a = (row0 + k) * kTX + col;
+            const float4 up = lds4(pa + a);
+            const float4 vv = lds4(pa + kTX * TY + a);
+            const float4 et = lds4(pa + 2 * kTX * TY + a);
+            const float4 uc = lds4(pu + k * BW);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float a = p.c[0] * xs[R + e];
-#pragma unroll
-              for (int r = 1; r <= R; ++r) {
-                const float s2 = (xs[R + e - r] + xs[R + e + r]) +
-                                 (get(w[R - r][k], e) + get(w[R + r][k], e));
-                a = fmaf(p.c[r], s2, a);
-              }
-              set(acc[k], e, a);
+              const float eta = get(et, e);
+              const float t = fmaf(get(vv, e), get(o[k], e),
+                                   fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
+              set(o[k], e, t / (1.0f + eta));
             }
           }
-          // y neighbours: every row within R of one of this thread's rows, each read once
-          // (rows of the thread itself come from the window).
+        }
 #pragma unroll
-          for (int h = -R; h < TYT + R; ++h) {
-            float4 v;
-            if (h >= 0 && h < TYT) v = w[R][h];
-            else v = lds4(pc + (row0 + h + R) * BW + kHX + col);
+        for (int k = 0; k < TYT; ++k) {
+          const int gy = y0 + row0 + k;
+          if (gy < p.ny - R && gx < p.nx) {
+            float* dst = p.out + ((size_t)z * p.ny + gy) * p.nx + gx;
+            if (gx >= R && gx + 4 <= p.nx - R) {
+              __stcs(reinterpret_cast<float4*>(dst), o[k]);
+            } else {
 #pragma unroll
-            for (int k = 0; k < TYT; ++k) {
-              const int d = h > k ? h - k : k - h;
-              if (d >= 1 && d <= R) {
-                acc[k].x = fmaf(p.c[d], v.x, acc[k].x);
-                acc[k].y = fmaf(p.c[d], v.y, acc[k].y);
-                acc[k].z = fmaf(p.c[d], v.z, acc[k].z);
-                acc[k].w = fmaf(p.c[d], v.w, acc[k].w);
-              }
+              for (int e = 0; e < 4; ++e)
+                if (gx + e >= R && gx + e < p.nx - R) dst[e] = get(o[k], e);
             }
           }
-
-          if constexpr (WAVE) {
-            if (!mbar_wait_bounded(base + 8u * (STAGES + J % ASTAGES), (J / ASTAGES) & 1)) fail(J);
-            const float* pa = auxr + (J % ASTAGES) * (C::kAuxStageBytes / 4);
-#pragma unroll
-            for (int k = 0; k < TYT; ++k) {
-              const int o = (row0 + k) * kTX + col;
-              const float4 up = lds4(pa + o);
-              const float4 vv = lds4(pa + kTX * TY + o);
-              const float4 et = lds4(pa + 2 * kTX * TY + o);
-              const float4 uc = w[R][k];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float eta = get(et, e);
-                const float t = fmaf(get(vv, e), get(acc[k], e),
-                                     fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
-                set(acc[k], e, t / (1.0f + eta));
-              }
-            }
-          }
-
-#pragma unroll
-          for (int k = 0; k < TYT; ++k) {
-            const int gy = y0 + row0 + k;
-            if (gy < p.ny - R && gx < p.nx) {
-              float* dst = p.out + ((size_t)z * p.ny + gy) * p.nx + gx;
-              if (gx >= R && gx + 4 <= p.nx - R) {
-                __stcs(reinterpret_cast<float4*>(dst), acc[k]);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  if (gx + e >= R && gx + e < p.nx - R) dst[e] = get(acc[k], e);
-              }
-            }
-          }
-
-          const bool stop = end_step(J);
-          ++J;
-          if (stop) goto drain;
         }
       }
+
+      // z filter, transposed form: every partial sum moves one slot down.
+#pragma unroll
+      for (int i = 1; i < 2 * R; ++i)
+#pragma unroll
+        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma4(p.c[i < R ? R - i : i - R], xv[k], s[i][k]);
+#pragma unroll
+      for (int k = 0; k < TYT; ++k) {
+        s[2 * R - 1][k].x = p.c[R] * xv[k].x;
+        s[2 * R - 1][k].y = p.c[R] * xv[k].y;
+        s[2 * R - 1][k].z = p.c[R] * xv[k].z;
+        s[2 * R - 1][k].w = p.c[R] * xv[k].w;
+      }
+
+      if (j >= R && j < L - R) {
+        // In-plane part of the landed plane's outputs; it emerges R planes later.
+        float4* acc = s[R - 1];
+#pragma unroll
+        for (int k = 0; k < TYT; ++k) {
+          const float* rowp = pl + own + k * BW;
+          float xs[4 + 2 * R];  // x = col-R .. col+3+R of this row
+          if constexpr (R >= 3) {
+            const float4 l = lds4(rowp - 4), r = lds4(rowp + 4);
+#pragma unroll
+            for (int e = 0; e < R; ++e) {
+              xs[R - 1 - e] = get(l, 3 - e);
+              xs[R + 4 + e] = get(r, e);
+            }
+          } else if constexpr (R == 2) {
+            const float2 l = *reinterpret_cast<const float2*>(rowp - 2);
+            const float2 r = *reinterpret_cast<const float2*>(rowp + 4);
+            xs[0] = l.x;
+            xs[1] = l.y;
+            xs[R + 4] = r.x;
+            xs[R + 5] = r.y;
+          } else {
+            xs[0] = rowp[-1];
+            xs[R + 4] = rowp[4];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) xs[R + e] = get(xv[k], e);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float a = get(acc[k], e);
+#pragma unroll
+            for (int r = 1; r <= R; ++r) a = fmaf(p.c[r], xs[R + e - r] + xs[R + e + r], a);
+            set(acc[k], e, a);
+          }
+        }
+        // y neighbours: rows within R of one of this thread's rows, each read once.
+#pragma unroll
+        for (int h = -R; h < TYT + R; ++h) {
+          const float4 v = (h >= 0 && h < TYT) ? xv[h >= 0 && h < TYT ? h : 0] : lds4(pl + own + h * BW);
+#pragma unroll
+          for (int k = 0; k < TYT; ++k) {
+            const int d = h > k ? h - k : k - h;
+            if (d >= 1 && d <= R) acc[k] = fma4(p.c[d], v, acc[k]);
+          }
+        }
+      }
+
+      // Close the step: every thread is done with the slot of plane (landed - KEEP).
+      const bool stop = __syncthreads_or(failed) != 0;
+      if (leader && !stop) {
+        fence_proxy_async_smem();
+        produce_u(J + STAGES - KEEP);
+        if (WAVE) produce_aux(J + ASTAGES);
+      }
+      ++J;
+      if (++slot == STAGES) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (WAVE && ++aslot == ASTAGES) {
+        aslot = 0;
+        aphase ^= 1u;
+      }
+      if (stop) goto drain;
     }
-  item_done:;
   }
   return;
 
