@@ -10,7 +10,7 @@ KernelDesc apply_kernel_desc(int radius) {
     case 1: return make_desc<1, 2, 16, 5, 1, false, 1>();
     case 2: return make_desc<2, 2, 16, 6, 1, false, 1>();
     case 3: return make_desc<3, 2, 16, 7, 1, false, 1>();
-    default: return make_desc<4, 2, 16, 8, 1, false, 1>();
+    default: return make_desc<4, 2, 16, 8, 1, false, 2>();
   }
 }
 

@@ -156,6 +156,34 @@ __device__ __forceinline__ float4 lds4(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
+// Four consecutive x values as two register pairs, for the packed fp32x2 arithmetic of
+// sm_100-family SMs (one FFMA2 performs two FMAs in one issue slot).
+struct P4 {
+  float2 a, b;  // (x0, x0+1), (x0+2, x0+3)
+};
+
+__device__ __forceinline__ P4 ldp4(const float* p) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  return P4{make_float2(v.x, v.y), make_float2(v.z, v.w)};
+}
+
+__device__ __forceinline__ float4 tof4(const P4& v) { return make_float4(v.a.x, v.a.y, v.b.x, v.b.y); }
+
+__device__ __forceinline__ P4 fma2x(const float2& c, const P4& x, const P4& y) {
+  return P4{__ffma2_rn(c, x.a, y.a), __ffma2_rn(c, x.b, y.b)};
+}
+
+__device__ __forceinline__ float pget(const P4& v, int e) {
+  return e == 0 ? v.a.x : e == 1 ? v.a.y : e == 2 ? v.b.x : v.b.y;
+}
+
+__device__ __forceinline__ void pset(P4& v, int e, float x) {
+  if (e == 0) v.a.x = x;
+  else if (e == 1) v.a.y = x;
+  else if (e == 2) v.b.x = x;
+  else v.b.y = x;
+}
+
 __device__ __forceinline__ float4 fma4(float a, const float4& x, const float4& y) {
   return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
 }
@@ -229,11 +257,14 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 
   if ((int)blockIdx.x >= p.nitems) return;
 
+  constexpr int NWARPS = C::kThreads / 32;
   const int tid = threadIdx.x;
   const int col = 4 * (tid % kThreadsX);     // x offset of this thread's float4 in the tile
   const int row0 = (tid / kThreadsX) * TYT;  // first tile row of this thread
   const int own = (row0 + R) * BW + kHX + col;  // its first point in a landed box
   const bool leader = tid == 0;
+  const int warp = tid >> 5;
+  const bool lane0 = (tid & 31) == 0;
 
   // Producer: stage the u box of the next plane in the cursor's sequence.
   auto produce_u = [&](int counter) {
@@ -295,35 +326,47 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   };
 
   // s[i][k]: partial sum of the output (i + 1 - R) planes after the current one, row k.
-  float4 s[2 * R][TYT];
+  P4 s[2 * R][TYT];
 #pragma unroll
   for (int i = 0; i < 2 * R; ++i)
 #pragma unroll
-    for (int k = 0; k < TYT; ++k) s[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < TYT; ++k) s[i][k] = P4{make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 cc[R + 1];  // coefficients duplicated into register pairs
+#pragma unroll
+  for (int r = 0; r <= R; ++r) cc[r] = make_float2(p.c[r], p.c[r]);
 
   int J = 0;               // load counter of the current step
   int slot = 0;            // J % STAGES
   uint32_t phase = 0;      // (J / STAGES) & 1
   int aslot = 0;           // J % ASTAGES
   uint32_t aphase = 0;     // (J / ASTAGES) & 1
+  int pwarp = 0;           // J % NWARPS: the warp that refills the ring after this step
+  const size_t plane = (size_t)p.nx * p.ny;
   for (int item = blockIdx.x; item < p.nitems; item += gridDim.x) {
     int x0, y0, za, zb;
     item_geometry<R, TY>(p, item, x0, y0, za, zb);
     const int L = zb - za + 2 * R;  // planes za-R .. zb+R-1 land in turn
     const int gx = x0 + col;
+    const int gy0 = y0 + row0;
+    // Output masks and row addresses of this thread, fixed for the whole item.
+    const bool vec_ok = gx >= R && gx + 4 <= p.nx - R;
+    bool row_ok[TYT];
+#pragma unroll
+    for (int k = 0; k < TYT; ++k) row_ok[k] = gy0 + k < p.ny - R && gx < p.nx;
+    float* const orow = p.out + (size_t)gy0 * p.nx + gx;
     for (int j = 0; j < L; ++j) {
       if (!mbar_wait_bounded(base + 8u * slot, phase)) fail(J);
       const float* pl = ring + slot * PSTRIDE;
-      float4 xv[TYT];
+      P4 xv[TYT];
 #pragma unroll
-      for (int k = 0; k < TYT; ++k) xv[k] = lds4(pl + own + k * BW);
+      for (int k = 0; k < TYT; ++k) xv[k] = ldp4(pl + own + k * BW);
 
       if (j >= 2 * R) {
         // Output plane z = (landed plane) - R is complete once its z part is added.
         const int z = za + j - 2 * R;
-        float4 o[TYT];
+        P4 o[TYT];
 #pragma unroll
-        for (int k = 0; k < TYT; ++k) o[k] = fma4(p.c[R], xv[k], s[0][k]);
+        for (int k = 0; k < TYT; ++k) o[k] = fma2x(cc[R], xv[k], s[0][k]);
         if constexpr (WAVE) {
           if (!mbar_wait_bounded(base + 8u * (STAGES + aslot), aphase)) fail(J);
           const float* pa = auxr + aslot * (C::kAuxStageBytes / 4);
@@ -340,23 +383,23 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float eta = get(et, e);
-              const float t = fmaf(get(vv, e), get(o[k], e),
+              const float t = fmaf(get(vv, e), pget(o[k], e),
                                    fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
-              set(o[k], e, t / (1.0f + eta));
+              pset(o[k], e, __fdividef(t, 1.0f + eta));  // 1 + eta in [1, 2]: 2-ulp divide
             }
           }
         }
+        float* const oz = orow + (size_t)z * plane;
 #pragma unroll
         for (int k = 0; k < TYT; ++k) {
-          const int gy = y0 + row0 + k;
-          if (gy < p.ny - R && gx < p.nx) {
-            float* dst = p.out + ((size_t)z * p.ny + gy) * p.nx + gx;
-            if (gx >= R && gx + 4 <= p.nx - R) {
-              __stcs(reinterpret_cast<float4*>(dst), o[k]);
+          if (row_ok[k]) {
+            float* dst = oz + k * p.nx;
+            if (vec_ok) {
+              __stcs(reinterpret_cast<float4*>(dst), tof4(o[k]));
             } else {
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                if (gx + e >= R && gx + e < p.nx - R) dst[e] = get(o[k], e);
+                if (gx + e >= R && gx + e < p.nx - R) dst[e] = pget(o[k], e);
             }
           }
         }
@@ -366,69 +409,75 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 #pragma unroll
       for (int i = 1; i < 2 * R; ++i)
 #pragma unroll
-        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma4(p.c[i < R ? R - i : i - R], xv[k], s[i][k]);
+        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma2x(cc[i < R ? R - i : i - R], xv[k], s[i][k]);
 #pragma unroll
-      for (int k = 0; k < TYT; ++k) {
-        s[2 * R - 1][k].x = p.c[R] * xv[k].x;
-        s[2 * R - 1][k].y = p.c[R] * xv[k].y;
-        s[2 * R - 1][k].z = p.c[R] * xv[k].z;
-        s[2 * R - 1][k].w = p.c[R] * xv[k].w;
-      }
+      for (int k = 0; k < TYT; ++k)
+        s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
 
       if (j >= R && j < L - R) {
         // In-plane part of the landed plane's outputs; it emerges R planes later.
-        float4* acc = s[R - 1];
+        P4* acc = s[R - 1];
 #pragma unroll
         for (int k = 0; k < TYT; ++k) {
           const float* rowp = pl + own + k * BW;
-          float xs[4 + 2 * R];  // x = col-R .. col+3+R of this row
+          // X[0..11]: x offsets -4..7 from this thread's first column, as register pairs
+          // L = X[0..3], C = X[4..7], Rt = X[8..11]; only the parts within R are loaded.
+          P4 Lq, Rq;
           if constexpr (R >= 3) {
-            const float4 l = lds4(rowp - 4), r = lds4(rowp + 4);
-#pragma unroll
-            for (int e = 0; e < R; ++e) {
-              xs[R - 1 - e] = get(l, 3 - e);
-              xs[R + 4 + e] = get(r, e);
-            }
+            Lq = ldp4(rowp - 4);
+            Rq = ldp4(rowp + 4);
           } else if constexpr (R == 2) {
-            const float2 l = *reinterpret_cast<const float2*>(rowp - 2);
-            const float2 r = *reinterpret_cast<const float2*>(rowp + 4);
-            xs[0] = l.x;
-            xs[1] = l.y;
-            xs[R + 4] = r.x;
-            xs[R + 5] = r.y;
+            Lq.b = *reinterpret_cast<const float2*>(rowp - 2);
+            Rq.a = *reinterpret_cast<const float2*>(rowp + 4);
           } else {
-            xs[0] = rowp[-1];
-            xs[R + 4] = rowp[4];
+            Lq.b.y = rowp[-1];
+            Rq.a.x = rowp[4];
           }
+          const P4& Cq = xv[k];
+          auto X = [&](int i) -> float {  // scalar X[i]
+            return i < 4 ? pget(Lq, i) : i < 8 ? pget(Cq, i - 4) : pget(Rq, i - 8);
+          };
+          auto XP = [&](int i) -> float2 {  // register pair X[i], X[i+1], i even
+            return i == 0 ? Lq.a : i == 2 ? Lq.b : i == 4 ? Cq.a : i == 6 ? Cq.b : i == 8 ? Rq.a : Rq.b;
+          };
 #pragma unroll
-          for (int e = 0; e < 4; ++e) xs[R + e] = get(xv[k], e);
+          for (int r = 1; r <= R; ++r) {
+            if (r % 2 == 0) {  // neighbour pairs stay register-aligned: packed
+              acc[k].a = __ffma2_rn(cc[r], __fadd2_rn(XP(4 - r), XP(4 + r)), acc[k].a);
+              acc[k].b = __ffma2_rn(cc[r], __fadd2_rn(XP(6 - r), XP(6 + r)), acc[k].b);
+            } else {  // odd distance: pairs straddle registers, scalar
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float a = get(acc[k], e);
-#pragma unroll
-            for (int r = 1; r <= R; ++r) a = fmaf(p.c[r], xs[R + e - r] + xs[R + e + r], a);
-            set(acc[k], e, a);
+              for (int e = 0; e < 4; ++e)
+                pset(acc[k], e, fmaf(p.c[r], X(4 + e - r) + X(4 + e + r), pget(acc[k], e)));
+            }
           }
         }
         // y neighbours: rows within R of one of this thread's rows, each read once.
 #pragma unroll
         for (int h = -R; h < TYT + R; ++h) {
-          const float4 v = (h >= 0 && h < TYT) ? xv[h >= 0 && h < TYT ? h : 0] : lds4(pl + own + h * BW);
+          const P4 v = (h >= 0 && h < TYT) ? xv[h >= 0 && h < TYT ? h : 0] : ldp4(pl + own + h * BW);
 #pragma unroll
           for (int k = 0; k < TYT; ++k) {
             const int d = h > k ? h - k : k - h;
-            if (d >= 1 && d <= R) acc[k] = fma4(p.c[d], v, acc[k]);
+            if (d >= 1 && d <= R) acc[k] = fma2x(cc[d], v, acc[k]);
           }
         }
       }
 
       // Close the step: every thread is done with the slot of plane (landed - KEEP).
+      // The refills rotate over the warps so that no warp carries them every step.
       const bool stop = __syncthreads_or(failed) != 0;
-      if (leader && !stop) {
-        fence_proxy_async_smem();
-        produce_u(J + STAGES - KEEP);
-        if (WAVE) produce_aux(J + ASTAGES);
+      if (lane0 && !stop) {
+        if (warp == pwarp) {
+          fence_proxy_async_smem();
+          produce_u(J + STAGES - KEEP);
+        }
+        if (WAVE && warp == (pwarp + NWARPS / 2) % NWARPS) {
+          fence_proxy_async_smem();
+          produce_aux(J + ASTAGES);
+        }
       }
+      if (++pwarp == NWARPS) pwarp = 0;
       ++J;
       if (++slot == STAGES) {
         slot = 0;
