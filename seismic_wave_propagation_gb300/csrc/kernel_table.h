@@ -22,27 +22,27 @@ struct KernelDesc {
   LaunchFn launch;
 };
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
                         const StarParams& p) {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
-  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB>
+  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB>
       <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, p);
   return cudaGetLastError();
 }
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1>
 KernelDesc make_desc() {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
-  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB>,
+  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB>,
                     C::kThreads,
                     C::kSmemBytes,
                     C::TY,
                     STAGES,
                     C::BW,
                     C::BH,
-                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB>};
+                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB>};
 }
 
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].

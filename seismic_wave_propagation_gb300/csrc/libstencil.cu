@@ -210,7 +210,7 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   }
   StarParams sp = p->params[kind];
   sp.out = out;
-  sp.debug_skip = p->debug_mode == 1 ? 2 * p->radius + 1 : -1;
+  sp.debug_skip = p->debug_mode == 1 ? 0 : -1;  // every CTA has a load 0
   // Copy the descriptors: the cache may evict entries while the launch is pending.
   const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me;
   cudaError_t e = kd.launch(dim3(p->grid[kind]), stream, a, b, c, d, sp);
@@ -417,3 +417,4 @@ int stencil_debug_inject(stencil_plan* p, int mode) {
 }
 
 }  // extern "C"
+

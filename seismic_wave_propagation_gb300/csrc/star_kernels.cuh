@@ -136,7 +136,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1; it < (1u << 28); ++it) {
+  for (uint32_t it = 1; it < (1u << 26); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
@@ -235,7 +235,7 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 
 // ---- the kernel ----------------------------------------------------------------------
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
@@ -340,7 +340,8 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   uint32_t phase = 0;      // (J / STAGES) & 1
   int aslot = 0;           // J % ASTAGES
   uint32_t aphase = 0;     // (J / ASTAGES) & 1
-  int pwarp = 0;           // J % NWARPS: the warp that refills the ring after this step
+  int pwarp = 0;           // the warp that refills the ring at the next barrier
+  int since = 0;           // steps since the last CTA barrier (one barrier per KB planes)
   const size_t plane = (size_t)p.nx * p.ny;
   for (int item = blockIdx.x; item < p.nitems; item += gridDim.x) {
     int x0, y0, za, zb;
@@ -464,20 +465,9 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         }
       }
 
-      // Close the step: every thread is done with the slot of plane (landed - KEEP).
-      // The refills rotate over the warps so that no warp carries them every step.
-      const bool stop = __syncthreads_or(failed) != 0;
-      if (lane0 && !stop) {
-        if (warp == pwarp) {
-          fence_proxy_async_smem();
-          produce_u(J + STAGES - KEEP);
-        }
-        if (WAVE && warp == (pwarp + NWARPS / 2) % NWARPS) {
-          fence_proxy_async_smem();
-          produce_aux(J + ASTAGES);
-        }
-      }
-      if (++pwarp == NWARPS) pwarp = 0;
+      // Close the step.  Every KB planes (and at the end of an item) the CTA meets at a
+      // barrier: every thread is then done with the slots of planes (landed - KEEP) of the
+      // steps since the last barrier, and one warp (rotating) refills them.
       ++J;
       if (++slot == STAGES) {
         slot = 0;
@@ -487,6 +477,20 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         aslot = 0;
         aphase ^= 1u;
       }
+      if (++since < KB && j + 1 < L) continue;
+      const bool stop = __syncthreads_or(failed) != 0;
+      if (lane0 && !stop) {
+        if (warp == pwarp) {
+          fence_proxy_async_smem();
+          for (int q = since; q > 0; --q) produce_u(J - q + STAGES - KEEP);
+        }
+        if (WAVE && warp == (pwarp + NWARPS / 2) % NWARPS) {
+          fence_proxy_async_smem();
+          for (int q = since; q > 0; --q) produce_aux(J - q + ASTAGES);
+        }
+      }
+      since = 0;
+      if (++pwarp == NWARPS) pwarp = 0;
       if (stop) goto drain;
     }
   }
@@ -495,14 +499,18 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 drain:
   // A wait ran out: make sure none of this CTA's copies is still landing in shared
   // memory before the CTA exits (bounded as well), then leave.
+  // Only the last STAGES (ASTAGES) loads issued can still be outstanding, one per slot.
   if (leader) {
-    for (int c = J > 0 ? J - 1 : 0; c < cur[0].issued; ++c)
+    const int nu = cur[0].issued;
+    for (int c = nu > STAGES ? nu - STAGES : 0; c < nu; ++c)
       if (c != p.debug_skip && !mbar_wait_bounded(base + 8u * (c % STAGES), (c / STAGES) & 1))
         atomicOr(p.status, kStatusDrainTimeout);
-    if (WAVE)
-      for (int c = J > 0 ? J - 1 : 0; c < cur[1].issued; ++c)
+    if (WAVE) {
+      const int na = cur[1].issued;
+      for (int c = na > ASTAGES ? na - ASTAGES : 0; c < na; ++c)
         if (!mbar_wait_bounded(base + 8u * (STAGES + c % ASTAGES), (c / ASTAGES) & 1))
           atomicOr(p.status, kStatusDrainTimeout);
+    }
   }
   __syncthreads();
 }
