@@ -134,6 +134,27 @@ int stencil_plan_launch_info(const stencil_plan* plan, int kind, int64_t* info, 
  */
 int stencil_debug_inject(stencil_plan* plan, int mode);
 
+/*
+ * Allocation-free stencil sweep.  No counterpart in the paper: it serves callers that
+ * cannot call cudaMalloc when they need a sweep (for example code running inside another
+ * framework's memory pool that owns the free device memory, or a process whose device
+ * memory footprint is fixed at start-up).  It computes exactly what
+ * stencil_plan_create + stencil_apply compute, with the same arguments, restrictions and
+ * error codes, and allocates nothing: no cudaMalloc/cudaFree, no heap, no plan.
+ *
+ * Scratch: the kernel's 16-byte status block lives in a file-scope device array of 256
+ * bytes that every GPU which loads the library holds until the process exits.  The need
+ * does not grow with the grid; grids beyond the library's maximum (each dimension
+ * <= 2^30, at most 2^40 points) are rejected with STENCIL_ERR_ARG.  The first call on a
+ * device looks up the array's device address (once per device, that device current);
+ * make that first call before any stream capture.  The call clears the status words,
+ * enqueues the sweep on `stream`, then synchronises `stream` so that it can report a
+ * device-side timeout (STENCIL_ERR_TIMEOUT).  Every call shares the one array per device:
+ * calls that overlap on the GPU (other host threads, other streams) race on it.
+ */
+int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int radius, const float* coeffs,
+                          const float* in, float* out, void* stream);
+
 /* Library version string. */
 const char* stencil_version(void);
 

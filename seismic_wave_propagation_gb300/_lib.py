@@ -181,3 +181,19 @@ class StencilPlan:
 
 def version() -> str:
     return load().stencil_version().decode()
+
+
+def apply_noalloc(nx: int, ny: int, nz: int, radius: int, coeffs, inp, out, stream=None) -> None:
+    """stencil_apply_noalloc: one sweep that allocates nothing on the device.
+
+    For callers that cannot allocate device memory when they need the sweep; its scratch
+    is a fixed 256-byte device array inside the library (see include/libstencil.h).
+    """
+    lib = load()
+    fn = lib.stencil_apply_noalloc
+    fn.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    c = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32))
+    _check(fn(int(nx), int(ny), int(nz), int(radius), c.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+              _addr(inp), _addr(out), _stream(stream, inp, out)))

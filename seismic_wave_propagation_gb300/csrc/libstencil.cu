@@ -418,3 +418,96 @@ int stencil_debug_inject(stencil_plan* p, int mode) {
 
 }  // extern "C"
 
+// ---- allocation-free sweep ---------------------------------------------------------
+//
+// Some callers cannot allocate device memory at the time they need a sweep: code that
+// runs inside another framework's memory pool which owns all free device memory, a
+// process with a fixed device-memory budget decided at start-up, or a host callback
+// where an allocation could deadlock with the caller's allocator.  For them,
+// stencil_apply_noalloc runs the same sweep kernel as stencil_apply, with the kernel's
+// status block placed in the file-scope device array below instead of plan-owned
+// memory, and builds its plan on the stack.
+//
+// In host code `g_noalloc_scratch` names a host-side stand-in, not the device copy:
+// passing it to a kernel would fault (or, where the GPU can reach host memory, silently
+// use the wrong memory).  Its device address is obtained with cudaGetSymbolAddress
+// once per device, with that device current, and cached.
+namespace {
+
+constexpr int kNoAllocScratchWords = 64;  // 256 bytes; the sweep uses the first 4 words
+__device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocScratchWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+int noalloc_scratch(int device, unsigned** out) {
+  if (device < 0 || device >= kMaxDevices)
+    return fail(STENCIL_ERR_ARG, "device ordinal %d beyond %d", device, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[device] = static_cast<unsigned*>(ptr);
+  }
+  *out = g_noalloc_ptr[device];
+  return STENCIL_OK;
+}
+
+}  // namespace
+
+extern "C" int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int radius,
+                                     const float* coeffs, const float* in, float* out,
+                                     void* stream) {
+  g_err[0] = 0;
+  if (radius < 1 || radius > STENCIL_MAX_RADIUS)
+    return fail(STENCIL_ERR_ARG, "radius %d outside [1, %d]", radius, STENCIL_MAX_RADIUS);
+  if (!coeffs) return fail(STENCIL_ERR_ARG, "coeffs is NULL");
+  if (nx < 1 || ny < 1 || nz < 1 || nx > (1 << 30) || ny > (1 << 30) || nz > (1 << 30) ||
+      nx * ny > ((int64_t)1 << 40) || nx * ny * nz > ((int64_t)1 << 40))
+    return fail(STENCIL_ERR_ARG,
+                "grid %lld x %lld x %lld beyond the maximum (each dimension <= 2^30, at most "
+                "2^40 points)",
+                (long long)nx, (long long)ny, (long long)nz);
+  if (nx % 4) return fail(STENCIL_ERR_ALIGNMENT, "nx = %lld is not a multiple of 4", (long long)nx);
+
+  stencil_plan pl{};  // on the stack: no heap or device allocation
+  pl.nx = nx;
+  pl.ny = ny;
+  pl.nz = nz;
+  pl.radius = radius;
+  for (int r = 0; r <= STENCIL_MAX_RADIUS; ++r) pl.c[r] = r <= radius ? coeffs[r] : 0.0f;
+  cudaError_t e = cudaGetDevice(&pl.device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  int rc = noalloc_scratch(pl.device, &pl.d_status);
+  if (rc) return rc;
+  pl.kd[0] = apply_kernel_desc(radius);
+  e = cudaFuncSetAttribute(pl.kd[0].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.kd[0].smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pl.occupancy[0], pl.kd[0].fn,
+                                                      pl.kd[0].threads, pl.kd[0].smem);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+  if (pl.occupancy[0] < 1) return fail(STENCIL_ERR_CUDA, "kernel cannot be resident (occupancy 0)");
+  plan_geometry(&pl, 0);
+
+  if ((rc = check_field(&pl, in, "in")) || (rc = check_field(&pl, out, "out"))) return rc;
+  if (overlap(in, out, (size_t)npoints(&pl) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
+
+  // The scratch keeps the previous call's contents: clear the status words first.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(pl.d_status, 0, 4 * sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_fail(e, "clear scratch");
+  if ((rc = launch(&pl, 0, in, nullptr, nullptr, nullptr, out, s))) return rc;
+  unsigned h[4] = {0, 0, 0, 0};
+  e = cudaMemcpyAsync(h, pl.d_status, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "sweep");
+  if (h[0] & kStatusBadSmem) return fail(STENCIL_ERR_CUDA, "shared memory base misaligned");
+  if (h[0])
+    return fail(STENCIL_ERR_TIMEOUT, "device wait for staged data ran out (flags 0x%x, block %u, load %u)",
+                h[0], h[1], h[2]);
+  return STENCIL_OK;
+}
