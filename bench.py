@@ -293,6 +293,19 @@ def run_ours(args, dist, rank, local, world):
             torch.cuda.synchronize(dev)
             wplan.status(s)
         wms = statistics.mean([x.elapsed_time(y) for x, y in wev])
+        # The same step with the region split (eta read only in the 16-point sponge).
+        with torch.cuda.stream(stream):
+            pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(wsteps)]
+            for i in range(wsteps):
+                pev[i][0].record(stream)
+                wplan.wave_step_pml(a.data_ptr(), b.data_ptr(), nxt.data_ptr(), f[2].data_ptr(),
+                                    f[3].data_ptr(), 16, s)
+                pev[i][1].record(stream)
+                a, b, nxt = b, nxt, a
+            torch.cuda.synchronize(dev)
+            wplan.status(s)
+        pms = statistics.mean([x.elapsed_time(y) for x, y in pev])
         wbytes = traffic.wave_bytes(n, n, n, R)
         wint = traffic.interior_points(n, n, n, R)
         wave = {"workload": "wave25_640", "steps": wsteps, "ms_per_step": wms,
@@ -300,7 +313,9 @@ def run_ours(args, dist, rank, local, world):
                 "roofline": {"bound": "hbm", "achieved": wbytes / (wms / 1e3) / 1e9, "peak": peak,
                              "unit": "GB/s", "frac": wbytes / (wms / 1e3) / 1e9 / peak,
                              "traffic": profiled_traffic("wave25_640")},
-                "launch": wplan.launch_info(1)}
+                "launch": wplan.launch_info(1),
+                "pml16": {"ms_per_step": pms, "gpoints_per_s": wint / (pms / 1e3) / 1e9,
+                          "wave_step_bytes_over_time_gbs": wbytes / (pms / 1e3) / 1e9}}
         wplan.close()
         del f, nxt, a, b
 
@@ -349,6 +364,113 @@ def run_ours(args, dist, rank, local, world):
         print(json.dumps(line), flush=True)
 
 
+def run_profile_case(kind: str):
+    """Three launches of the 512^3 case of one kernel: the driver for ncu captures."""
+    import torch
+    from seismic_wave_propagation_gb300 import StencilPlan
+    n = NX
+    c = synth.laplacian8_coeffs()
+    plan = StencilPlan(n, n, n, R, c)
+    if kind == "sweep":
+        u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
+        o = u.clone()
+        for _ in range(3):
+            plan.apply(u, o)
+    else:
+        f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(n, n, n)]
+        nxt = f[0].clone()
+        for _ in range(3):
+            plan.wave_step(f[0], f[1], nxt, f[2], f[3])
+    torch.cuda.synchronize()
+    plan.status()
+    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info(0 if kind == "sweep" else 1)}))
+
+
+def _time_loop(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_report_configs(args):
+    """Time all five workloads as their configs define them (sweeps/steps loops), plus the
+    CPU oracle on a bounded sample of each; one JSON line per workload and a markdown table."""
+    import torch
+    from seismic_wave_propagation_gb300 import StencilPlan
+    peak, _ = peaks()
+    stream = torch.cuda.Stream()
+    out = []
+    for name, w in synth.WORKLOADS.items():
+        nx, ny, nz, r = w["nx"], w["ny"], w["nz"], w["radius"]
+        c = synth.coeffs_for(w["coeffs"])
+        plan = StencilPlan(nx, ny, nz, r, c)
+        interior = traffic.interior_points(nx, ny, nz, r)
+        with torch.cuda.stream(stream):
+            if w["init"] == "wave":
+                f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(nx, ny, nz)]
+                bufs = [f[0], f[1], f[0].clone()]
+                v, e = f[2], f[3]
+
+                def loop():
+                    for _ in range(w["steps"]):
+                        plan.wave_step(bufs[0], bufs[1], bufs[2], v, e, stream)
+                        bufs[0], bufs[1], bufs[2] = bufs[1], bufs[2], bufs[0]
+                units, per = w["steps"], traffic.wave_bytes(nx, ny, nz, r)
+            else:
+                u0 = synth.sinusoid_field(nx, ny, nz) if w["init"] == "sinusoids" else synth.uniform_field(nx, ny, nz)
+                a = torch.from_numpy(u0.ravel()).cuda()
+                bufs = [a, a.clone()]
+                nsw = w["sweeps"]
+
+                def loop():
+                    for _ in range(nsw):
+                        plan.apply(bufs[0], bufs[1], stream)
+                        bufs[0], bufs[1] = bufs[1], bufs[0]
+                units, per = nsw, traffic.apply_bytes(nx, ny, nz, r)
+            reps = max(1, min(101, int(2000 // max(1, units))))
+            ms = _time_loop(loop, reps, 3, stream)
+            plan.status(stream)
+        ms_unit = ms / units
+        line = {"workload": name, "grid": [nx, ny, nz], "radius": r, "units": units,
+                "ms_per_sweep_or_step": ms_unit, "gpoints_per_s": interior / (ms_unit / 1e3) / 1e9,
+                "hbm_gbs": per / (ms_unit / 1e3) / 1e9, "frac_of_peak": per / (ms_unit / 1e3) / 1e9 / peak,
+                "timed_loops": reps}
+        if not args.skip_cpu:
+            import oracle
+            oracle.build()
+            cc = c.astype(np.float32)
+            planes = max(2 * r + 1, min(nz, 2 * r + max(1, int(4e7 // max(1, nx * ny)))))
+            if w["init"] == "wave":
+                sub = [np.ascontiguousarray(x[:planes]) for x in synth.wave_fields(nx, ny, planes)]
+                t0 = time.perf_counter()
+                oracle.wave_step(sub[0], sub[1], sub[2], sub[3], cc, r)
+            else:
+                sub = np.ascontiguousarray(synth.uniform_field(nx, ny, planes))
+                t0 = time.perf_counter()
+                oracle.apply(sub, cc, r)
+            dt = time.perf_counter() - t0
+            line["cpu_oracle_gpoints_per_s"] = traffic.interior_points(nx, ny, planes, r) / dt / 1e9
+            line["cpu_cores"] = oracle.num_threads()
+        print(json.dumps(line), flush=True)
+        out.append(line)
+        plan.close()
+        del bufs
+        torch.cuda.empty_cache()
+    print("| workload | GPoints/s | HBM GB/s | % of measured peak | ms per sweep/step | CPU oracle GPoints/s |")
+    print("|---|---|---|---|---|---|")
+    for l in out:
+        print(f"| {l['workload']} | {l['gpoints_per_s']:.1f} | {l['hbm_gbs']:.0f} | {100 * l['frac_of_peak']:.1f} | "
+              f"{l['ms_per_sweep_or_step']:.4f} | {l.get('cpu_oracle_gpoints_per_s', float('nan')):.2f} |")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -358,7 +480,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
+    ap.add_argument("--profile", choices=["sweep", "wave"], help="run 3 launches of the 512^3 case (ncu driver)")
+    ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
+    if args.profile or args.report_configs:
+        from seismic_wave_propagation_gb300 import build as b
+        b.build()
+        if args.profile:
+            run_profile_case(args.profile)
+        else:
+            run_report_configs(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     dist, rank, local, world = dist_setup(args.gpus)

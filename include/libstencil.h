@@ -91,6 +91,21 @@ int wave_step(stencil_plan* plan, const float* u_prev, const float* u, float* u_
               const float* v2dt2, const float* eta, void* stream);
 
 /*
+ * The same wave step for a model whose damping lives in a band of `pml_width` points
+ * along the six faces ("Accelerating High-Order Stencils on GPUs" runs the inner region
+ * and the PML region as separate data regions).  Precondition: eta = 0 at every point at
+ * least pml_width away from all faces.  The call then skips staging eta and the divide by
+ * 1+eta for every (64 x tile-height) output tile and plane that lies wholly in that
+ * region, where the update is the plain leapfrog u_next = 2u - u_prev + v2dt2*lap(u), so
+ * the inner region moves 16 instead of 20 bytes per point; tiles that reach into the band
+ * use eta as given.  If the precondition does not hold, points outside the band are
+ * computed with eta taken as 0 or as given, depending on their tile.  Same fields, layout,
+ * aliasing rules and errors as wave_step; pml_width >= 0.
+ */
+int wave_step_pml(stencil_plan* plan, const float* u_prev, const float* u, float* u_next,
+                  const float* v2dt2, const float* eta, int64_t pml_width, void* stream);
+
+/*
  * Synchronise `stream`, then report device-side failures of this plan's kernels since
  * the previous call: STENCIL_ERR_TIMEOUT if a kernel's bounded wait for staged data ran
  * out (its outputs are then undefined), STENCIL_ERR_CUDA on a CUDA error, else STENCIL_OK.
@@ -119,7 +134,8 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
                   const float* v2dt2_host, const float* eta_host, int nsteps, void* stream);
 
 /*
- * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step), written
+ * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step,
+ * 2 = wave_step_pml), written
  * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
  * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
  * Returns the number of values written, or a negative error code.

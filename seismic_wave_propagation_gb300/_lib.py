@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "libstencil.h")
 STENCIL_OK = 0
 ERRORS = {-1: "STENCIL_ERR_ARG", -2: "STENCIL_ERR_ALIGNMENT", -3: "STENCIL_ERR_ALIAS",
           -4: "STENCIL_ERR_CUDA", -5: "STENCIL_ERR_TIMEOUT"}
-KIND_APPLY, KIND_WAVE = 0, 1
+KIND_APPLY, KIND_WAVE, KIND_WAVE_PML = 0, 1, 2
 LAUNCH_INFO_KEYS = ("grid", "threads", "smem", "ctas_per_sm", "tiles", "zchunks", "tile_x",
                     "tile_y", "stages", "sms")
 
@@ -58,6 +58,7 @@ def load():
         lib.stencil_plan_destroy.restype = None
         lib.stencil_apply.argtypes = [vp, vp, vp, vp]
         lib.wave_step.argtypes = [vp] * 7
+        lib.wave_step_pml.argtypes = [vp] * 6 + [i64, vp]
         lib.stencil_plan_status.argtypes = [vp, vp]
         lib.stencil_last_error.restype = ctypes.c_char_p
         lib.stencil_apply_host.argtypes = [vp, vp, vp, ctypes.c_int, vp]
@@ -65,7 +66,7 @@ def load():
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
         lib.stencil_version.restype = ctypes.c_char_p
-        for fn in ("stencil_apply", "wave_step", "stencil_plan_status", "stencil_apply_host",
+        for fn in ("stencil_apply", "wave_step", "wave_step_pml", "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
@@ -155,6 +156,11 @@ class StencilPlan:
     def wave_step(self, u_prev, u, u_next, v2dt2, eta, stream=None) -> None:
         fields = (u_prev, u, u_next, v2dt2, eta)
         _check(self._lib.wave_step(self._p, *[_addr(f) for f in fields], _stream(stream, *fields)))
+
+    def wave_step_pml(self, u_prev, u, u_next, v2dt2, eta, pml_width: int, stream=None) -> None:
+        fields = (u_prev, u, u_next, v2dt2, eta)
+        _check(self._lib.wave_step_pml(self._p, *[_addr(f) for f in fields], int(pml_width),
+                                       _stream(stream, *fields)))
 
     def status(self, stream=None, *fields) -> None:
         _check(self._lib.stencil_plan_status(self._p, _stream(stream, *fields)))

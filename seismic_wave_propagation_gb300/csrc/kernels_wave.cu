@@ -6,7 +6,15 @@
 
 namespace libstencil {
 
-KernelDesc wave_kernel_desc(int radius) {
+KernelDesc wave_kernel_desc(int radius, bool pml) {
+  if (pml) {
+    switch (radius) {
+      case 1: return make_desc<1, 1, 16, 5, 3, true, 2, 1, true>();
+      case 2: return make_desc<2, 1, 16, 6, 3, true, 2, 1, true>();
+      case 3: return make_desc<3, 1, 16, 7, 3, true, 2, 1, true>();
+      default: return make_desc<4, 1, 16, 8, 3, true, 2, 1, true>();
+    }
+  }
   switch (radius) {
     case 1: return make_desc<1, 1, 16, 5, 3, true, 2>();
     case 2: return make_desc<2, 1, 16, 6, 3, true, 2>();

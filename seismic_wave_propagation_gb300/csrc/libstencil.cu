@@ -12,7 +12,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/libstencil.h"
+#include "libstencil.h"
 #include "kernel_table.h"
 
 using namespace libstencil;
@@ -67,10 +67,10 @@ struct stencil_plan {
   float c[STENCIL_MAX_RADIUS + 1];
   int device;
   int num_sms;
-  KernelDesc kd[2];    // [0] apply, [1] wave
-  int occupancy[2];    // CTAs per SM
-  StarParams params[2];
-  int grid[2];
+  KernelDesc kd[3];    // [0] apply, [1] wave, [2] wave with eta in a face band
+  int occupancy[3];    // CTAs per SM
+  StarParams params[3];
+  int grid[3];
   unsigned* d_status;  // 4 words
   MapEntry maps[kMapCache];
   uint64_t clock;
@@ -195,13 +195,13 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
 }
 
 int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
-           const float* eta, float* out, cudaStream_t stream) {
+           const float* eta, float* out, cudaStream_t stream, int pml = 1 << 30) {
   if (p->grid[kind] == 0) return STENCIL_OK;  // empty interior: nothing to do
   const KernelDesc& kd = p->kd[kind];
   const CUtensorMap *mu, *mp = nullptr, *mv = nullptr, *me = nullptr;
   int rc = get_map(p, u, kd.box_w, kd.box_h, &mu);
   if (rc) return rc;
-  if (kind == 1) {
+  if (kind >= 1) {
     if ((rc = get_map(p, uprev, kTX, kd.tile_y, &mp))) return rc;
     if ((rc = get_map(p, v2dt2, kTX, kd.tile_y, &mv))) return rc;
     if ((rc = get_map(p, eta, kTX, kd.tile_y, &me))) return rc;
@@ -210,6 +210,7 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   }
   StarParams sp = p->params[kind];
   sp.out = out;
+  sp.pml = pml;
   sp.debug_skip = p->debug_mode == 1 ? 0 : -1;  // every CTA has a load 0
   // Copy the descriptors: the cache may evict entries while the launch is pending.
   const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me;
@@ -274,8 +275,9 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
     return nullptr;
   }
   p->kd[0] = apply_kernel_desc(radius);
-  p->kd[1] = wave_kernel_desc(radius);
-  for (int k = 0; k < 2; ++k) {
+  p->kd[1] = wave_kernel_desc(radius, false);
+  p->kd[2] = wave_kernel_desc(radius, true);
+  for (int k = 0; k < 3; ++k) {
     e = cudaFuncSetAttribute(p->kd[k].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->kd[k].smem);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p->occupancy[k], p->kd[k].fn,
@@ -323,6 +325,26 @@ int wave_step(stencil_plan* p, const float* u_prev, const float* u, float* u_nex
   if (u_next != u_prev && overlap(u_next, u_prev, bytes))
     return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
   return launch(p, 1, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream));
+}
+
+int wave_step_pml(stencil_plan* p, const float* u_prev, const float* u, float* u_next,
+                  const float* v2dt2, const float* eta, int64_t pml_width, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (pml_width < 0) return fail(STENCIL_ERR_ARG, "pml_width < 0");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, u_prev, "u_prev")) || (rc = check_field(p, u, "u")) ||
+      (rc = check_field(p, u_next, "u_next")) || (rc = check_field(p, v2dt2, "v2dt2")) ||
+      (rc = check_field(p, eta, "eta")))
+    return rc;
+  const size_t bytes = (size_t)npoints(p) * 4;
+  if (overlap(u_next, u, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps u");
+  if (overlap(u_next, v2dt2, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps v2dt2");
+  if (overlap(u_next, eta, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps eta");
+  if (u_next != u_prev && overlap(u_next, u_prev, bytes))
+    return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
+  const int pml = (int)std::min<int64_t>(pml_width, 1 << 30);
+  return launch(p, 2, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream), pml);
 }
 
 int stencil_plan_status(stencil_plan* p, void* stream) {
@@ -400,7 +422,7 @@ int wave_run_host(stencil_plan* p, float* u_prev_host, float* u_host, const floa
 }
 
 int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int n) {
-  if (!p || !info || n < 0 || kind < 0 || kind > 1) return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (!p || !info || n < 0 || kind < 0 || kind > 2) return fail(STENCIL_ERR_ARG, "bad arguments");
   const KernelDesc& kd = p->kd[kind];
   const StarParams& sp = p->params[kind];
   const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.ntiles,

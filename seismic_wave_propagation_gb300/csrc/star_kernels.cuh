@@ -55,6 +55,7 @@ struct StarParams {
   float* out;       // stencil output, or u_next for the wave step
   unsigned* status; // [0] flags, [1] block, [2] load counter of the first failure
   int debug_skip;   // load counter every CTA skips (watchdog test); -1 = none
+  int pml;          // wave step with a face band: eta is zero beyond `pml` points from the faces
 };
 
 // Producer cursor (kept in shared memory, touched by the elected thread only).
@@ -214,6 +215,14 @@ __device__ __forceinline__ void item_geometry(const StarParams& p, int item, int
   zb = R + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
 }
 
+// Does the wave step need eta for the output tile at (x0, y0), plane z?  Only where the
+// tile reaches into the band of `pml` points along the faces; elsewhere eta is zero.
+template <int TY>
+__device__ __forceinline__ bool tile_needs_eta(const StarParams& p, int x0, int y0, int z) {
+  return z < p.pml || z >= p.nz - p.pml || x0 < p.pml || x0 + kTX > p.nx - p.pml || y0 < p.pml ||
+         y0 + TY > p.ny - p.pml;
+}
+
 template <int R, int TY>
 __device__ __forceinline__ void cursor_set_item(const StarParams& p, Cursor& k, int item) {
   k.item = item;
@@ -235,7 +244,7 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 
 // ---- the kernel ----------------------------------------------------------------------
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
@@ -289,10 +298,11 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     if (k.j >= 2 * R) {
       const uint32_t dst = aux_base + slot * C::kAuxStageBytes;
       const int z = k.za + k.j - 2 * R;
-      mbar_arrive_expect_tx(bar, C::kAuxStageBytes);
+      const bool eta = !PML || tile_needs_eta<TY>(p, k.x0, k.y0, z);
+      mbar_arrive_expect_tx(bar, (eta ? 3 : 2) * C::kAuxFieldBytes);
       tma_load_3d(dst, &tm_uprev, bar, k.x0, k.y0, z);
       tma_load_3d(dst + C::kAuxFieldBytes, &tm_v2dt2, bar, k.x0, k.y0, z);
-      tma_load_3d(dst + 2 * C::kAuxFieldBytes, &tm_eta, bar, k.x0, k.y0, z);
+      if (eta) tma_load_3d(dst + 2 * C::kAuxFieldBytes, &tm_eta, bar, k.x0, k.y0, z);
     } else {
       mbar_arrive(bar);  // filling step: nothing to stage, just complete the phase
     }
@@ -374,19 +384,32 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
           int cs = slot - R;
           if (cs < 0) cs += STAGES;
           const float* pu = ring + cs * PSTRIDE + own;  // u at plane z (landed R steps ago)
+          if (!PML || tile_needs_eta<TY>(p, x0, y0, z)) {
 #pragma unroll
-          for (int k = 0; k < TYT; ++k) {
-            const int a = (row0 + k) * kTX + col;
-            const float4 up = lds4(pa + a);
-            const float4 vv = lds4(pa + kTX * TY + a);
-            const float4 et = lds4(pa + 2 * kTX * TY + a);
-            const float4 uc = lds4(pu + k * BW);
+            for (int k = 0; k < TYT; ++k) {
+              const int a = (row0 + k) * kTX + col;
+              const float4 up = lds4(pa + a);
+              const float4 vv = lds4(pa + kTX * TY + a);
+              const float4 et = lds4(pa + 2 * kTX * TY + a);
+              const float4 uc = lds4(pu + k * BW);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float eta = get(et, e);
-              const float t = fmaf(get(vv, e), pget(o[k], e),
-                                   fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
-              pset(o[k], e, __fdividef(t, 1.0f + eta));  // 1 + eta in [1, 2]: 2-ulp divide
+              for (int e = 0; e < 4; ++e) {
+                const float eta = get(et, e);
+                const float t = fmaf(get(vv, e), pget(o[k], e),
+                                     fmaf(-(1.0f - eta), get(up, e), 2.0f * get(uc, e)));
+                pset(o[k], e, __fdividef(t, 1.0f + eta));  // 1 + eta in [1, 2]: 2-ulp divide
+              }
+            }
+          } else {  // the tile lies where eta = 0: plain leapfrog, no eta staged, no divide
+#pragma unroll
+            for (int k = 0; k < TYT; ++k) {
+              const int a = (row0 + k) * kTX + col;
+              const float4 up = lds4(pa + a);
+              const float4 vv = lds4(pa + kTX * TY + a);
+              const float4 uc = lds4(pu + k * BW);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                pset(o[k], e, fmaf(get(vv, e), pget(o[k], e), fmaf(2.0f, get(uc, e), -get(up, e))));
             }
           }
         }

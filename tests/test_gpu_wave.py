@@ -127,3 +127,60 @@ def test_wave25_640_hundred_steps():
     r = rel_l2(g_cur, o_cur)
     print(f"wave25 640^3 x100: relative L2 {r:.3e}, |u|_2 {np.linalg.norm(o_cur):.4f}")
     assert r <= 1e-4
+
+
+def band_mask(shape, width):
+    """True at points closer than `width` to a face."""
+    nz, ny, nx = shape
+    d = np.minimum.reduce(np.meshgrid(np.minimum(np.arange(nz), nz - 1 - np.arange(nz)),
+                                      np.minimum(np.arange(ny), ny - 1 - np.arange(ny)),
+                                      np.minimum(np.arange(nx), nx - 1 - np.arange(nx)), indexing="ij"))
+    return d < width
+
+
+@pytest.mark.parametrize("pml,dims", [(16, (200, 150, 90)), (10, (136, 75, 41)), (0, (136, 75, 41)),
+                                      (1000, (136, 75, 41)), (5, (96, 70, 60))])
+def test_wave_step_pml_matches_oracle(pml, dims):
+    """Region-split step on fields whose eta vanishes beyond `pml` points from the faces
+    (random inside the band): identical to the full update, which the oracle computes."""
+    torch = torch_cuda()
+    nx, ny, nz = dims
+    c = synth.laplacian8_coeffs()
+    c32 = c.astype(np.float32)
+    up = synth.uniform_field(nx, ny, nz, seed=21)
+    u = synth.uniform_field(nx, ny, nz, seed=22)
+    s = synth.uniform_field(nx, ny, nz, seed=23, scale=0.05) + np.float32(0.1)
+    e = synth.uniform_field(nx, ny, nz, seed=24, scale=0.05) + np.float32(0.05)
+    e = np.where(band_mask(u.shape, pml), e, np.float32(0.0)).astype(np.float32)
+    plan = StencilPlan(nx, ny, nz, 4, c)
+    d = [torch.from_numpy(a.ravel()).cuda() for a in (up, u, s, e)]
+    nxt = torch.full_like(d[0], 7.0)
+    plan.wave_step_pml(d[0], d[1], nxt, d[2], d[3], pml)
+    plan.status(None, nxt)
+    got = nxt.cpu().numpy().reshape(u.shape)
+    want = oracle.wave_step(up, u, s, e, c32, 4, u_next=np.full_like(u, 7.0))
+    m = interior_mask(u.shape, 4)
+    assert np.max(np.abs(got[m] - want[m])) <= 1e-5 * (2 + 0.15 * 19.51) * 2
+    assert np.all(got[~m] == 7.0)
+    plan.close()
+
+
+def test_wave_step_pml_on_the_sponge_model_equals_wave_step():
+    """On the sponge model (eta = 0 beyond 16 points) the split step reproduces wave_step."""
+    torch = torch_cuda()
+    n = 96
+    up, u, s, e = synth.wave_fields(n, n, n)
+    c = synth.laplacian8_coeffs()
+    plan = StencilPlan(n, n, n, 4, c)
+    d = [torch.from_numpy(a.ravel()).cuda() for a in (up, u, s, e)]
+    a, b = d[0].clone(), d[1].clone()
+    ap, bp = d[0].clone(), d[1].clone()
+    for _ in range(20):
+        plan.wave_step(a, b, a, d[2], d[3])
+        a, b = b, a
+        plan.wave_step_pml(ap, bp, ap, d[2], d[3], 16)
+        ap, bp = bp, ap
+    plan.status(None, a)
+    g, gp = b.cpu().numpy(), bp.cpu().numpy()
+    assert rel_l2(gp, g.astype(np.float64)) <= 1e-6
+    plan.close()
