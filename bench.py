@@ -419,10 +419,8 @@ def run_report_configs(args):
                 bufs = [f[0], f[1], f[0].clone()]
                 v, e = f[2], f[3]
 
-                def loop():
-                    for _ in range(w["steps"]):
-                        plan.wave_step(bufs[0], bufs[1], bufs[2], v, e, stream)
-                        bufs[0], bufs[1], bufs[2] = bufs[1], bufs[2], bufs[0]
+                def loop():  # the workload's step loop, one graph launch
+                    plan.wave_steps(bufs[0], bufs[1], bufs[2], v, e, w["steps"], -1, True, stream)
                 units, per = w["steps"], traffic.wave_bytes(nx, ny, nz, r)
             else:
                 u0 = synth.sinusoid_field(nx, ny, nz) if w["init"] == "sinusoids" else synth.uniform_field(nx, ny, nz)
@@ -430,10 +428,8 @@ def run_report_configs(args):
                 bufs = [a, a.clone()]
                 nsw = w["sweeps"]
 
-                def loop():
-                    for _ in range(nsw):
-                        plan.apply(bufs[0], bufs[1], stream)
-                        bufs[0], bufs[1] = bufs[1], bufs[0]
+                def loop():  # the workload's ping-pong sweeps, one graph launch
+                    plan.sweeps(bufs[0], bufs[1], nsw, True, stream)
                 units, per = nsw, traffic.apply_bytes(nx, ny, nz, r)
             reps = max(1, min(101, int(2000 // max(1, units))))
             ms = _time_loop(loop, reps, 3, stream)

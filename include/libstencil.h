@@ -106,6 +106,27 @@ int wave_step_pml(stencil_plan* plan, const float* u_prev, const float* u, float
                   const float* v2dt2, const float* eta, int64_t pml_width, void* stream);
 
 /*
+ * Time loops on device buffers (hot-path loop row: sweeps and steps back to back on one
+ * stream, as the benchmark workloads run them).
+ *
+ * stencil_sweeps: `nsweeps` ping-pong sweeps a -> b -> a -> ...; after an even count the
+ *   result is in a, after an odd count in b.  Both buffers keep their shells (start them
+ *   as two copies of the same field for a fixed boundary).  a and b must not overlap.
+ * wave_steps: `nsteps` wave steps with three-buffer rotation: each step computes the next
+ *   level into the buffer of the oldest one, so after n steps the newest level is in
+ *   (u_prev, u, u_tmp)[(n + 1) % 3] and the one before it in [n % 3].  pml_width < 0 uses
+ *   wave_step, pml_width >= 0 wave_step_pml.  The three levels must not overlap each other,
+ *   v2dt2 or eta.
+ * use_graph != 0 records the launches once into a CUDA graph (cached in the plan for the
+ *   same buffers and count) and replays it, which removes the per-launch host cost.  The
+ *   first call with a new key captures on a private stream; do not call it while `stream`
+ *   itself is being captured.  Errors as for stencil_apply / wave_step.
+ */
+int stencil_sweeps(stencil_plan* plan, float* a, float* b, int nsweeps, int use_graph, void* stream);
+int wave_steps(stencil_plan* plan, float* u_prev, float* u, float* u_tmp, const float* v2dt2,
+               const float* eta, int nsteps, int64_t pml_width, int use_graph, void* stream);
+
+/*
  * Synchronise `stream`, then report device-side failures of this plan's kernels since
  * the previous call: STENCIL_ERR_TIMEOUT if a kernel's bounded wait for staged data ran
  * out (its outputs are then undefined), STENCIL_ERR_CUDA on a CUDA error, else STENCIL_OK.

@@ -60,13 +60,16 @@ def load():
         lib.wave_step.argtypes = [vp] * 7
         lib.wave_step_pml.argtypes = [vp] * 6 + [i64, vp]
         lib.stencil_plan_status.argtypes = [vp, vp]
+        lib.stencil_sweeps.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, vp]
+        lib.wave_steps.argtypes = [vp] * 6 + [ctypes.c_int, i64, ctypes.c_int, vp]
         lib.stencil_last_error.restype = ctypes.c_char_p
         lib.stencil_apply_host.argtypes = [vp, vp, vp, ctypes.c_int, vp]
         lib.wave_run_host.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
         lib.stencil_version.restype = ctypes.c_char_p
-        for fn in ("stencil_apply", "wave_step", "wave_step_pml", "stencil_plan_status", "stencil_apply_host",
+        for fn in ("stencil_apply", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
+                   "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
@@ -161,6 +164,18 @@ class StencilPlan:
         fields = (u_prev, u, u_next, v2dt2, eta)
         _check(self._lib.wave_step_pml(self._p, *[_addr(f) for f in fields], int(pml_width),
                                        _stream(stream, *fields)))
+
+    def sweeps(self, a, b, nsweeps: int, use_graph: bool = False, stream=None) -> None:
+        """stencil_sweeps: ping-pong sweeps a -> b -> a ...; odd counts end in b."""
+        _check(self._lib.stencil_sweeps(self._p, _addr(a), _addr(b), int(nsweeps), int(use_graph),
+                                        _stream(stream, a, b)))
+
+    def wave_steps(self, u_prev, u, u_tmp, v2dt2, eta, nsteps: int, pml_width: int = -1,
+                   use_graph: bool = False, stream=None) -> None:
+        """wave_steps: three-buffer rotation; the newest level ends in [(n+1) % 3]."""
+        fields = (u_prev, u, u_tmp, v2dt2, eta)
+        _check(self._lib.wave_steps(self._p, *[_addr(f) for f in fields], int(nsteps), int(pml_width),
+                                    int(use_graph), _stream(stream, *fields)))
 
     def status(self, stream=None, *fields) -> None:
         _check(self._lib.stencil_plan_status(self._p, _stream(stream, *fields)))

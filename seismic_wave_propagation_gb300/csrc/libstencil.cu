@@ -77,6 +77,9 @@ struct stencil_plan {
   float* work;         // host-API workspace
   size_t work_floats;
   int debug_mode;
+  // Cached CUDA graph of the last multi-launch loop (stencil_sweeps / wave_steps).
+  cudaGraphExec_t graph;
+  uint64_t graph_key[8];
 };
 
 namespace {
@@ -232,6 +235,47 @@ int ensure_work(stencil_plan* p, size_t floats) {
 
 }  // namespace
 
+namespace {
+
+// Enqueue `body` (a sequence of launches on `s`) directly, or as a CUDA graph captured
+// once per distinct key and replayed afterwards.
+template <class Body>
+int run_loop(stencil_plan* p, const uint64_t key[8], bool use_graph, cudaStream_t s, Body body) {
+  if (!use_graph) return body(s);
+  if (!p->graph || std::memcmp(key, p->graph_key, sizeof p->graph_key) != 0) {
+    if (p->graph) {
+      cudaGraphExecDestroy(p->graph);
+      p->graph = nullptr;
+    }
+    cudaStream_t cap;
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "capture stream");
+    e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    int rc = STENCIL_OK;
+    if (e == cudaSuccess) rc = body(cap);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e2 = cudaStreamEndCapture(cap, &g);
+    cudaStreamDestroy(cap);
+    if (e != cudaSuccess) return cuda_fail(e, "begin capture");
+    if (rc) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    if (e2 != cudaSuccess) return cuda_fail(e2, "end capture");
+    e = cudaGraphInstantiate(&p->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      p->graph = nullptr;
+      return cuda_fail(e, "graph instantiate");
+    }
+    std::memcpy(p->graph_key, key, sizeof p->graph_key);
+  }
+  cudaError_t e = cudaGraphLaunch(p->graph, s);
+  return e == cudaSuccess ? STENCIL_OK : cuda_fail(e, "graph launch");
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* stencil_last_error(void) { return g_err; }
@@ -295,6 +339,7 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
 
 void stencil_plan_destroy(stencil_plan* p) {
   if (!p) return;
+  if (p->graph) cudaGraphExecDestroy(p->graph);
   if (p->d_status) cudaFree(p->d_status);
   if (p->work) cudaFree(p->work);
   delete p;
@@ -345,6 +390,67 @@ int wave_step_pml(stencil_plan* p, const float* u_prev, const float* u, float* u
     return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
   const int pml = (int)std::min<int64_t>(pml_width, 1 << 30);
   return launch(p, 2, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream), pml);
+}
+
+int stencil_sweeps(stencil_plan* p, float* a, float* b, int nsweeps, int use_graph, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (nsweeps < 0) return fail(STENCIL_ERR_ARG, "nsweeps < 0");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, a, "a")) || (rc = check_field(p, b, "b"))) return rc;
+  if (overlap(a, b, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "a and b overlap");
+  const uint64_t key[8] = {1, (uint64_t)(uintptr_t)a, (uint64_t)(uintptr_t)b, (uint64_t)nsweeps,
+                           (uint64_t)p->debug_mode, 0, 0, 0};
+  return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+    float* x = a;
+    float* y = b;
+    for (int i = 0; i < nsweeps; ++i) {
+      const int r = launch(p, 0, x, nullptr, nullptr, nullptr, y, s);
+      if (r) return r;
+      std::swap(x, y);
+    }
+    return (int)STENCIL_OK;
+  });
+}
+
+int wave_steps(stencil_plan* p, float* u_prev, float* u, float* u_tmp, const float* v2dt2,
+               const float* eta, int nsteps, int64_t pml_width, int use_graph, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (nsteps < 0) return fail(STENCIL_ERR_ARG, "nsteps < 0");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, u_prev, "u_prev")) || (rc = check_field(p, u, "u")) ||
+      (rc = check_field(p, u_tmp, "u_tmp")) || (rc = check_field(p, v2dt2, "v2dt2")) ||
+      (rc = check_field(p, eta, "eta")))
+    return rc;
+  const size_t bytes = (size_t)npoints(p) * 4;
+  const float* bufs[3] = {u_prev, u, u_tmp};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(bufs[i], bufs[j], bytes)) return fail(STENCIL_ERR_ALIAS, "time levels overlap");
+    if (overlap(bufs[i], v2dt2, bytes) || overlap(bufs[i], eta, bytes))
+      return fail(STENCIL_ERR_ALIAS, "a time level overlaps v2dt2 or eta");
+  }
+  const int kind = pml_width >= 0 ? 2 : 1;
+  const int pml = pml_width >= 0 ? (int)std::min<int64_t>(pml_width, 1 << 30) : (1 << 30);
+  const uint64_t key[8] = {2, (uint64_t)(uintptr_t)u_prev, (uint64_t)(uintptr_t)u,
+                           (uint64_t)(uintptr_t)u_tmp, (uint64_t)(uintptr_t)v2dt2,
+                           (uint64_t)(uintptr_t)eta, ((uint64_t)nsteps << 32) | (uint32_t)pml,
+                           (uint64_t)p->debug_mode};
+  return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
+    float* x = u_prev;
+    float* y = u;
+    float* z = u_tmp;
+    for (int i = 0; i < nsteps; ++i) {
+      const int r = launch(p, kind, y, x, v2dt2, eta, z, s, pml);
+      if (r) return r;
+      float* t = x;  // rotate: (prev, cur, next) <- (cur, next, prev)
+      x = y;
+      y = z;
+      z = t;
+    }
+    return (int)STENCIL_OK;
+  });
 }
 
 int stencil_plan_status(stencil_plan* p, void* stream) {

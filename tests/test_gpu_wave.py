@@ -184,3 +184,29 @@ def test_wave_step_pml_on_the_sponge_model_equals_wave_step():
     g, gp = b.cpu().numpy(), bp.cpu().numpy()
     assert rel_l2(gp, g.astype(np.float64)) <= 1e-6
     plan.close()
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+@pytest.mark.parametrize("pml", [-1, 16])
+def test_native_step_loop_matches_step_by_step(use_graph, pml):
+    torch = torch_cuda()
+    n, steps = 80, 7
+    up, u, s, e = synth.wave_fields(n, n, n)
+    c = synth.laplacian8_coeffs()
+    plan = StencilPlan(n, n, n, 4, c)
+    f = [torch.from_numpy(x.ravel()).cuda() for x in (up, u, s, e)]
+    for _ in range(2):  # the second call replays the cached graph
+        bufs = [f[0].clone(), f[1].clone(), f[0].clone()]
+        plan.wave_steps(bufs[0], bufs[1], bufs[2], f[2], f[3], steps, pml_width=pml, use_graph=use_graph)
+        plan.status(None, bufs[0])
+    a, b, t = f[0].clone(), f[1].clone(), f[0].clone()
+    for _ in range(steps):
+        if pml < 0:
+            plan.wave_step(a, b, t, f[2], f[3])
+        else:
+            plan.wave_step_pml(a, b, t, f[2], f[3], pml)
+        a, b, t = b, t, a
+    plan.status(None, a)
+    assert torch.equal(bufs[(steps + 1) % 3], b)
+    assert torch.equal(bufs[steps % 3], a)
+    plan.close()
