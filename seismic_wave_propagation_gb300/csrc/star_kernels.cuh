@@ -476,14 +476,16 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
             }
           }
         }
-        // y neighbours: rows within R of one of this thread's rows, each read once.
+        // y neighbours in symmetric pairs (k-d, k+d): one add, one FMA per pair.
 #pragma unroll
-        for (int h = -R; h < TYT + R; ++h) {
-          const P4 v = (h >= 0 && h < TYT) ? xv[h >= 0 && h < TYT ? h : 0] : ldp4(pl + own + h * BW);
+        for (int d = 1; d <= R; ++d) {
 #pragma unroll
           for (int k = 0; k < TYT; ++k) {
-            const int d = h > k ? h - k : k - h;
-            if (d >= 1 && d <= R) acc[k] = fma2x(cc[d], v, acc[k]);
+            const int hm = k - d, hp = k + d;
+            const P4 vm = (hm >= 0 && hm < TYT) ? xv[hm >= 0 && hm < TYT ? hm : 0] : ldp4(pl + own + hm * BW);
+            const P4 vp = (hp >= 0 && hp < TYT) ? xv[hp >= 0 && hp < TYT ? hp : 0] : ldp4(pl + own + hp * BW);
+            acc[k].a = __ffma2_rn(cc[d], __fadd2_rn(vm.a, vp.a), acc[k].a);
+            acc[k].b = __ffma2_rn(cc[d], __fadd2_rn(vm.b, vp.b), acc[k].b);
           }
         }
       }
