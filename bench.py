@@ -192,7 +192,7 @@ def run_reference(args, dist, rank, world):
     u = synth.uniform_field(NX, NY, NZ)
     import oracle
     oracle.build()
-    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    per_step = min(args.cpu_budget, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(u, c, per_step)
     vals, samples = [], []
