@@ -145,7 +145,9 @@ const char* stencil_last_error(void);
  * reported as STENCIL_ERR_TIMEOUT.
  *
  * stencil_apply_host: out_host = `nsweeps` ping-pong sweeps of in_host with a fixed
- *   shell (the shell of out_host equals that of in_host).  nsweeps >= 0.
+ *   shell (the shell of out_host equals that of in_host).  nsweeps >= 0.  A single sweep
+ *   is pipelined over z-slabs on three internal streams (copy in, sweep, copy out), so
+ *   both copy directions and the sweep overlap; use pinned host memory to benefit.
  * wave_run_host: `nsteps` wave steps from (u_prev_host, u_host); on return
  *   u_prev_host and u_host hold the last two time levels (u_host the newest).
  */

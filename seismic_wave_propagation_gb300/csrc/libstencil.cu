@@ -80,6 +80,10 @@ struct stencil_plan {
   // Cached CUDA graph of the last multi-launch loop (stencil_sweeps / wave_steps).
   cudaGraphExec_t graph;
   uint64_t graph_key[8];
+  // Streams and events of the slab-pipelined host-buffer sweep (created on first use).
+  cudaStream_t pipe[3];  // copies in, compute, copies out
+  cudaEvent_t ev[2 * 32 + 2];
+  bool pipe_ready;
 };
 
 namespace {
@@ -91,11 +95,11 @@ bool interior_empty(const stencil_plan* p) {
   return p->nx < m || p->ny < m || p->nz < m;
 }
 
-// Choose the number of z-chunks per tile column: minimise the per-CTA step count of the
+// Launch geometry for the output planes [R + zoff, R + zoff + nzi) of the grid.  Choose
+// the number of z-chunks per tile column: minimise the per-CTA step count of the
 // round-robin schedule (a filling step costs about a third of a computing one).
-void plan_geometry(stencil_plan* p, int kind) {
+void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp, int& grid) {
   const KernelDesc& kd = p->kd[kind];
-  StarParams& sp = p->params[kind];
   const int R = p->radius;
   std::memset(&sp, 0, sizeof sp);
   sp.nx = (int)p->nx;
@@ -104,14 +108,15 @@ void plan_geometry(stencil_plan* p, int kind) {
   for (int r = 0; r <= 4; ++r) sp.c[r] = r <= R ? p->c[r] : 0.0f;
   sp.status = p->d_status;
   sp.debug_skip = -1;
-  if (interior_empty(p)) {
-    p->grid[kind] = 0;
+  if (interior_empty(p) || nzi <= 0) {
+    grid = 0;
     return;
   }
   sp.ntx = (int)((p->nx + kTX - 1) / kTX);
   const int nty = (int)((p->ny - 2 * R + kd.tile_y - 1) / kd.tile_y);
   sp.ntiles = sp.ntx * nty;
-  sp.nzi = (int)(p->nz - 2 * R);
+  sp.nzi = nzi;
+  sp.zoff = zoff;
   const int64_t slots = (int64_t)p->num_sms * std::max(1, p->occupancy[kind]);
   double best = 1e300;
   int best_n = 1;
@@ -129,7 +134,11 @@ void plan_geometry(stencil_plan* p, int kind) {
   }
   sp.nchunks = best_n;
   sp.nitems = sp.ntiles * best_n;
-  p->grid[kind] = (int)std::min<int64_t>(sp.nitems, slots);
+  grid = (int)std::min<int64_t>(sp.nitems, slots);
+}
+
+void plan_geometry(stencil_plan* p, int kind) {
+  geometry(p, kind, 0, (int)(p->nz - 2 * p->radius), p->params[kind], p->grid[kind]);
 }
 
 int check_device(const stencil_plan* p) {
@@ -197,9 +206,15 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   return STENCIL_OK;
 }
 
+// Launch one sweep (kind 0) or wave step (1, 2).  nzi >= 0 restricts it to the output
+// planes [R + zoff, R + zoff + nzi).
 int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
-           const float* eta, float* out, cudaStream_t stream, int pml = 1 << 30) {
-  if (p->grid[kind] == 0) return STENCIL_OK;  // empty interior: nothing to do
+           const float* eta, float* out, cudaStream_t stream, int pml = 1 << 30, int zoff = 0,
+           int nzi = -1) {
+  StarParams sp = p->params[kind];
+  int grid = p->grid[kind];
+  if (nzi >= 0) geometry(p, kind, zoff, nzi, sp, grid);
+  if (grid == 0) return STENCIL_OK;  // empty interior: nothing to do
   const KernelDesc& kd = p->kd[kind];
   const CUtensorMap *mu, *mp = nullptr, *mv = nullptr, *me = nullptr;
   int rc = get_map(p, u, kd.box_w, kd.box_h, &mu);
@@ -211,13 +226,12 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   } else {
     mp = mv = me = mu;
   }
-  StarParams sp = p->params[kind];
   sp.out = out;
   sp.pml = pml;
   sp.debug_skip = p->debug_mode == 1 ? 0 : -1;  // every CTA has a load 0
   // Copy the descriptors: the cache may evict entries while the launch is pending.
   const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me;
-  cudaError_t e = kd.launch(dim3(p->grid[kind]), stream, a, b, c, d, sp);
+  cudaError_t e = kd.launch(dim3(grid), stream, a, b, c, d, sp);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return STENCIL_OK;
 }
@@ -272,6 +286,65 @@ int run_loop(stencil_plan* p, const uint64_t key[8], bool use_graph, cudaStream_
   }
   cudaError_t e = cudaGraphLaunch(p->graph, s);
   return e == cudaSuccess ? STENCIL_OK : cuda_fail(e, "graph launch");
+}
+
+}  // namespace
+
+namespace {
+
+// One sweep from host to host, pipelined over z-slabs on three streams so that the copy
+// in of later slabs, the sweep of the current one and the copy out of earlier ones
+// overlap.  Slab k computes output planes [z_k, z_k+1); it needs input planes up to
+// z_k+1 + R - 1, which the copy-in chunks [p_k, p_k+1) with p_k = z_k + R deliver in
+// order.  Its output chunk [o_k, o_k+1) (o_k = z_k, widened to the grid's first and last
+// planes at the ends) is first filled from the input (the shell), then swept, then
+// copied out.
+int apply_host_pipelined(stencil_plan* p, const float* in_host, float* out_host, float* a, float* b,
+                         cudaStream_t user) {
+  const int R = p->radius;
+  const int nz = (int)p->nz;
+  const int nzi = nz - 2 * R;
+  const size_t plane = (size_t)p->nx * p->ny;
+  cudaError_t e = cudaSuccess;
+  if (!p->pipe_ready) {
+    for (cudaStream_t& q : p->pipe)
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking);
+    for (cudaEvent_t& v : p->ev)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "pipeline streams");
+    p->pipe_ready = true;
+  }
+  const int K = std::max(1, std::min(32, nzi / 32));
+  auto zk = [&](int k) { return R + (int)(((int64_t)k * nzi) / K); };
+  auto pk = [&](int k) { return k == 0 ? 0 : k == K ? nz : zk(k) + R; };
+  auto ok = [&](int k) { return k == 0 ? 0 : k == K ? nz : zk(k); };
+  cudaStream_t hin = p->pipe[0], comp = p->pipe[1], hout = p->pipe[2];
+  cudaEvent_t start = p->ev[2 * 32], done = p->ev[2 * 32 + 1];
+  e = cudaEventRecord(start, user);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hin, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hout, start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
+  for (int k = 0; k < K; ++k) {
+    cudaEvent_t landed = p->ev[k], swept = p->ev[32 + k];
+    const size_t i0 = (size_t)pk(k) * plane, i1 = (size_t)pk(k + 1) * plane;
+    const size_t o0 = (size_t)ok(k) * plane, o1 = (size_t)ok(k + 1) * plane;
+    e = cudaMemcpyAsync(a + i0, in_host + i0, (i1 - i0) * 4, cudaMemcpyHostToDevice, hin);
+    if (e == cudaSuccess) e = cudaEventRecord(landed, hin);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, landed, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(b + o0, a + o0, (o1 - o0) * 4, cudaMemcpyDeviceToDevice, comp);
+    if (e != cudaSuccess) return cuda_fail(e, "pipelined copy in");
+    const int rc = launch(p, 0, a, nullptr, nullptr, nullptr, b, comp, 1 << 30, zk(k) - R, zk(k + 1) - zk(k));
+    if (rc) return rc;
+    e = cudaEventRecord(swept, comp);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hout, swept, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out_host + o0, b + o0, (o1 - o0) * 4, cudaMemcpyDeviceToHost, hout);
+    if (e != cudaSuccess) return cuda_fail(e, "pipelined copy out");
+  }
+  e = cudaEventRecord(done, hout);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(user, done, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pipeline end");
+  return stencil_plan_status(p, user);
 }
 
 }  // namespace
@@ -340,6 +413,10 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
 void stencil_plan_destroy(stencil_plan* p) {
   if (!p) return;
   if (p->graph) cudaGraphExecDestroy(p->graph);
+  if (p->pipe_ready) {
+    for (cudaStream_t q : p->pipe) cudaStreamDestroy(q);
+    for (cudaEvent_t v : p->ev) cudaEventDestroy(v);
+  }
   if (p->d_status) cudaFree(p->d_status);
   if (p->work) cudaFree(p->work);
   delete p;
@@ -485,6 +562,7 @@ int stencil_apply_host(stencil_plan* p, const float* in_host, float* out_host, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* a = p->work;
   float* b = p->work + n;
+  if (nsweeps == 1 && !interior_empty(p)) return apply_host_pipelined(p, in_host, out_host, a, b, s);
   cudaError_t e = cudaMemcpyAsync(a, in_host, n * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && nsweeps > 0) e = cudaMemcpyAsync(b, a, n * 4, cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "copy in");

@@ -48,7 +48,8 @@ struct StarParams {
   int nx, ny, nz;
   int ntx;          // tiles along x
   int ntiles;       // tiles per plane
-  int nzi;          // interior planes (nz - 2R)
+  int nzi;          // output planes of this launch (nz - 2R for the whole grid)
+  int zoff;         // first output plane of this launch minus R (0 for the whole grid)
   int nchunks;      // z chunks per tile column
   int nitems;       // ntiles * nchunks
   float c[5];       // c[0] total centre weight, c[r] per-neighbour weight
@@ -211,8 +212,8 @@ __device__ __forceinline__ void item_geometry(const StarParams& p, int item, int
   const int bx = tile - by * p.ntx;
   x0 = bx * kTX;
   y0 = R + by * TY;
-  za = R + (int)(((long long)chunk * p.nzi) / p.nchunks);
-  zb = R + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
+  za = R + p.zoff + (int)(((long long)chunk * p.nzi) / p.nchunks);
+  zb = R + p.zoff + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
 }
 
 // Does the wave step need eta for the output tile at (x0, y0), plane z?  Only where the

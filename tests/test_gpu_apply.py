@@ -206,3 +206,22 @@ def test_native_sweep_loop_matches_launch_by_launch(use_graph, nsweeps):
     got = a if nsweeps % 2 == 0 else b
     assert torch.equal(got, x)
     plan.close()
+
+
+@pytest.mark.parametrize("dims,R", [((136, 75, 200), 4), ((64, 40, 140), 1), ((32, 32, 20), 4)])
+def test_pipelined_host_sweep_matches_device_path(dims, R):
+    """One host-to-host sweep runs pipelined over z-slabs; it must equal the device path."""
+    torch = torch_cuda()
+    nx, ny, nz = dims
+    c = synth.laplacian8_coeffs()[:R + 1] if R == 4 else synth.laplacian2_coeffs()
+    u = synth.uniform_field(nx, ny, nz, seed=77)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    out_h = np.full_like(u, 3.0)
+    for _ in range(2):
+        plan.apply_host(u, out_h, 1)
+    a = torch.from_numpy(u.ravel()).cuda()
+    b = a.clone()
+    plan.apply(a, b)
+    plan.status(None, b)
+    np.testing.assert_array_equal(out_h.ravel(), b.cpu().numpy())
+    plan.close()
