@@ -12,9 +12,11 @@
 //     z-major order, so CTAs working on neighbouring tiles march through the same planes
 //     at the same time and their halos are served from L2.
 //   * Each plane's (64+8) x (TY+2R) box is staged into a shared-memory ring by TMA
-//     (cp.async.bulk.tensor.3d), one elected thread issuing, completion tracked by an
-//     mbarrier per slot (expect-tx bytes).  Out-of-range box parts are zero-filled by
-//     the TMA unit and only ever feed outputs that are masked off.
+//     (cp.async.bulk.tensor.3d), completion tracked by an mbarrier per slot (expect-tx
+//     bytes).  The CTA meets at one barrier per plane; right after it, lane 0 of one warp
+//     (the duty rotates over the warps) refills the slot the plane just released.
+//     Out-of-range box parts are zero-filled by the TMA unit and only ever feed outputs
+//     that are masked off.
 //   * Every thread owns a 4 x TYT block of output columns (one float4 per row).  Along z
 //     it runs the symmetric 2R+1-tap filter h_i = c_|i-R| in transposed form: when plane
 //     p lands, its own values x update 2R running partial sums,
@@ -59,7 +61,8 @@ struct StarParams {
   int pml;          // wave step with a face band: eta is zero beyond `pml` points from the faces
 };
 
-// Producer cursor (kept in shared memory, touched by the elected thread only).
+// Producer cursor: the next load of the CTA's sequence (kept in shared memory; the warps
+// that refill the ring take turns, and the CTA barrier between turns orders them).
 struct Cursor {
   int item, j, L, x0, y0, za, issued, pad;
 };
@@ -76,8 +79,7 @@ struct StarCfg {
   static constexpr int kAuxStageBytes = 3 * kAuxFieldBytes;
   static constexpr int kNumBars = STAGES + (WAVE ? ASTAGES : 0);
   static constexpr int kCurOff = (8 * kNumBars + 15) / 16 * 16;
-  static constexpr int kFlagOff = kCurOff + 2 * (int)sizeof(Cursor);
-  static constexpr int kRingOffset = (kFlagOff + 16 + 127) / 128 * 128;
+  static constexpr int kRingOffset = (kCurOff + 2 * (int)sizeof(Cursor) + 127) / 128 * 128;
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
   static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
   static constexpr int KEEP = WAVE ? R : 0;             // planes kept behind the lead
@@ -186,19 +188,8 @@ __device__ __forceinline__ void pset(P4& v, int e, float x) {
   else v.b.y = x;
 }
 
-__device__ __forceinline__ float4 fma4(float a, const float4& x, const float4& y) {
-  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
-}
-
 __device__ __forceinline__ float get(const float4& v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ void set(float4& v, int e, float a) {
-  if (e == 0) v.x = a;
-  else if (e == 1) v.y = a;
-  else if (e == 2) v.z = a;
-  else v.w = a;
 }
 
 // ---- work decomposition -------------------------------------------------------------

@@ -250,3 +250,29 @@ def test_grid_beyond_2pow31_points():
     last = b[(nz - 1) * nx * ny:].cpu().numpy()
     assert np.all(last == 5.0)  # the shell's last plane is untouched
     plan.close()
+
+
+def test_two_plans_on_two_streams_concurrently():
+    """Plans own their state; sweeps of two plans overlapping on two streams are unaffected."""
+    torch = torch_cuda()
+    dims = [(136, 75, 120, 4), (200, 64, 90, 1)]
+    plans, ins, outs, refs = [], [], [], []
+    for nx, ny, nz, R in dims:
+        c = synth.laplacian8_coeffs() if R == 4 else synth.laplacian2_coeffs()
+        u = synth.uniform_field(nx, ny, nz, seed=nx + R)
+        plans.append(StencilPlan(nx, ny, nz, R, c))
+        ins.append(torch.from_numpy(u.ravel()).cuda())
+        outs.append(ins[-1].clone())
+        ref = ins[-1].clone()
+        plans[-1].apply(ins[-1], ref)
+        plans[-1].status(None, ref)
+        refs.append(ref)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for p, a, b, s in zip(plans, ins, outs, streams):
+            p.apply(a, b, s)
+    for p, b, ref, s in zip(plans, outs, refs, streams):
+        p.status(s)
+        assert torch.equal(b, ref)
+        p.close()
