@@ -421,18 +421,12 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         }
       }
 
-      // z filter, transposed form: every partial sum moves one slot down.
-#pragma unroll
-      for (int i = 1; i < 2 * R; ++i)
-#pragma unroll
-        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma2x(cc[i < R ? R - i : i - R], xv[k], s[i][k]);
-#pragma unroll
-      for (int k = 0; k < TYT; ++k)
-        s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
-
       if (j >= R && j < L - R) {
-        // In-plane part of the landed plane's outputs; it emerges R planes later.
-        P4* acc = s[R - 1];
+        // In-plane part of the landed plane's outputs.  Before the z filter below runs,
+        // s[R] holds that plane's partial sums; the filter's FMA then carries them on
+        // (they emerge R planes later).  Doing this part first measured 7 % faster than
+        // after the filter: the loads issue earlier and the FMA chains overlap better.
+        P4* acc = s[R];
 #pragma unroll
         for (int k = 0; k < TYT; ++k) {
           const float* rowp = pl + own + k * BW;
@@ -481,6 +475,15 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
           }
         }
       }
+
+      // z filter, transposed form: every partial sum moves one slot down.
+#pragma unroll
+      for (int i = 1; i < 2 * R; ++i)
+#pragma unroll
+        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma2x(cc[i < R ? R - i : i - R], xv[k], s[i][k]);
+#pragma unroll
+      for (int k = 0; k < TYT; ++k)
+        s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
 
       // Close the step.  Every KB planes (and at the end of an item) the CTA meets at a
       // barrier: every thread is then done with the slots of planes (landed - KEEP) of the
