@@ -371,11 +371,11 @@ def run_profile_case(kind: str):
     n = NX
     c = synth.laplacian8_coeffs()
     plan = StencilPlan(n, n, n, R, c)
-    if kind == "sweep":
+    if kind in ("sweep", "semi"):
         u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
         o = u.clone()
         for _ in range(3):
-            plan.apply(u, o)
+            (plan.apply if kind == "sweep" else plan.apply_semi)(u, o)
     else:
         f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(n, n, n)]
         nxt = f[0].clone()
@@ -383,7 +383,7 @@ def run_profile_case(kind: str):
             plan.wave_step(f[0], f[1], nxt, f[2], f[3])
     torch.cuda.synchronize()
     plan.status()
-    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info(0 if kind == "sweep" else 1)}))
+    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info({"sweep": 0, "wave": 1, "semi": 3}[kind])}))
 
 
 def _time_loop(fn, steps, warmup, stream):
@@ -460,11 +460,34 @@ def run_report_configs(args):
         plan.close()
         del bufs
         torch.cuda.empty_cache()
+    # The two sweep kernels side by side: the transposed z filter (stencil_apply) and the
+    # semi-stencil form (stencil_apply_semi), single launches at 512^3 (inputs > L2).
+    n = 512
+    u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
+    o = u.clone()
+    cmp = []
+    for r in (1, 4):
+        plan = StencilPlan(n, n, n, r, synth.laplacian8_coeffs() if r == 4 else synth.laplacian2_coeffs())
+        per = traffic.apply_bytes(n, n, n, r)
+        row = {"comparison": f"sweep R={r} {n}^3"}
+        with torch.cuda.stream(stream):
+            for label, fn in (("transposed", plan.apply), ("semi", plan.apply_semi)):
+                ms = _time_loop(lambda: fn(u, o, stream), 200, 10, stream)
+                row[label] = {"ms": ms, "hbm_gbs": per / (ms / 1e3) / 1e9, "frac_of_peak": per / (ms / 1e3) / 1e9 / peak}
+            plan.status(stream)
+        print(json.dumps(row), flush=True)
+        cmp.append(row)
+        plan.close()
     print("| workload | GPoints/s | HBM GB/s | % of measured peak | ms per sweep/step | CPU oracle GPoints/s |")
     print("|---|---|---|---|---|---|")
     for l in out:
         print(f"| {l['workload']} | {l['gpoints_per_s']:.1f} | {l['hbm_gbs']:.0f} | {100 * l['frac_of_peak']:.1f} | "
               f"{l['ms_per_sweep_or_step']:.4f} | {l.get('cpu_oracle_gpoints_per_s', float('nan')):.2f} |")
+    print("| sweep kernel | transposed z filter: ms, % of peak | semi-stencil: ms, % of peak |")
+    print("|---|---|---|")
+    for row in cmp:
+        t, m = row["transposed"], row["semi"]
+        print(f"| {row['comparison']} | {t['ms']:.4f}, {100 * t['frac_of_peak']:.1f} | {m['ms']:.4f}, {100 * m['frac_of_peak']:.1f} |")
 
 
 def main():
@@ -476,7 +499,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
-    ap.add_argument("--profile", choices=["sweep", "wave"], help="run 3 launches of the 512^3 case (ncu driver)")
+    ap.add_argument("--profile", choices=["sweep", "wave", "semi"], help="run 3 launches of the 512^3 case (ncu driver)")
     ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
     if args.profile or args.report_configs:

@@ -75,6 +75,19 @@ void stencil_plan_destroy(stencil_plan* plan);
 int stencil_apply(stencil_plan* plan, const float* in, float* out, void* stream);
 
 /*
+ * The same sweep computed in semi-stencil form ("Accelerating High-Order Stencils on
+ * GPUs", the semi-stencil strategy: a stencil along one axis is split into a forward and
+ * a backward half, so the centre and one half are read together and the other half is
+ * carried as a partial result).  Along z, the centre and the R planes below each output
+ * plane are read from shared memory (the ring keeps them), and the R planes above
+ * finish a running partial sum held in registers, R partial sums per point instead of
+ * 2R.  Same result up to fp32 rounding order, same arguments, layout, aliasing rules and
+ * errors as stencil_apply.  An alternative kernel for comparison: stencil_apply is the
+ * faster one on GB300.
+ */
+int stencil_apply_semi(stencil_plan* plan, const float* in, float* out, void* stream);
+
+/*
  * One time step of the acoustic isotropic wave equation with a sponge layer, fused
  * into a single pass (the stencil of the plan is the Laplacian, h = 1):
  *   u_next = (2*u - (1 - eta)*u_prev + v2dt2 * lap(u)) / (1 + eta)
@@ -158,7 +171,7 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
 
 /*
  * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step,
- * 2 = wave_step_pml), written
+ * 2 = wave_step_pml, 3 = stencil_apply_semi), written
  * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
  * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
  * Returns the number of values written, or a negative error code.

@@ -6,9 +6,9 @@ The compute path is the CUDA shared library ``libstencil.so`` (sm_103a) built fr
 Importing the package does not load the library; the first plan does, and raises if it
 has not been built.
 """
-from ._lib import (KIND_APPLY, KIND_WAVE, StencilError, StencilPlan, last_error, load,  # noqa: F401
-                   version)
+from ._lib import (KIND_APPLY, KIND_SEMI, KIND_WAVE, KIND_WAVE_PML, StencilError, StencilPlan,  # noqa: F401
+                   last_error, load, version)
 from . import synth, traffic  # noqa: F401
 
-__all__ = ["StencilPlan", "StencilError", "KIND_APPLY", "KIND_WAVE", "load", "last_error",
+__all__ = ["StencilPlan", "StencilError", "KIND_APPLY", "KIND_WAVE", "KIND_WAVE_PML", "KIND_SEMI", "load", "last_error",
            "version", "synth", "traffic"]

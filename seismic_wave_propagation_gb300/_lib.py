@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "libstencil.h")
 STENCIL_OK = 0
 ERRORS = {-1: "STENCIL_ERR_ARG", -2: "STENCIL_ERR_ALIGNMENT", -3: "STENCIL_ERR_ALIAS",
           -4: "STENCIL_ERR_CUDA", -5: "STENCIL_ERR_TIMEOUT"}
-KIND_APPLY, KIND_WAVE, KIND_WAVE_PML = 0, 1, 2
+KIND_APPLY, KIND_WAVE, KIND_WAVE_PML, KIND_SEMI = 0, 1, 2, 3
 LAUNCH_INFO_KEYS = ("grid", "threads", "smem", "ctas_per_sm", "tiles", "zchunks", "tile_x",
                     "tile_y", "stages", "sms")
 
@@ -57,6 +57,7 @@ def load():
         lib.stencil_plan_destroy.argtypes = [vp]
         lib.stencil_plan_destroy.restype = None
         lib.stencil_apply.argtypes = [vp, vp, vp, vp]
+        lib.stencil_apply_semi.argtypes = [vp, vp, vp, vp]
         lib.wave_step.argtypes = [vp] * 7
         lib.wave_step_pml.argtypes = [vp] * 6 + [i64, vp]
         lib.stencil_plan_status.argtypes = [vp, vp]
@@ -68,7 +69,7 @@ def load():
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
         lib.stencil_version.restype = ctypes.c_char_p
-        for fn in ("stencil_apply", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
+        for fn in ("stencil_apply", "stencil_apply_semi", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
                    "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -155,6 +156,10 @@ class StencilPlan:
 
     def apply(self, inp, out, stream=None) -> None:
         _check(self._lib.stencil_apply(self._p, _addr(inp), _addr(out), _stream(stream, inp, out)))
+
+    def apply_semi(self, inp, out, stream=None) -> None:
+        """The same sweep in semi-stencil form (an alternative kernel; see the header)."""
+        _check(self._lib.stencil_apply_semi(self._p, _addr(inp), _addr(out), _stream(stream, inp, out)))
 
     def wave_step(self, u_prev, u, u_next, v2dt2, eta, stream=None) -> None:
         fields = (u_prev, u, u_next, v2dt2, eta)

@@ -22,32 +22,36 @@ struct KernelDesc {
   LaunchFn launch;
 };
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1, bool PML = false>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
+          bool PML = false, bool SEMI = false>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
                         const StarParams& p) {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
-  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML>
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
+  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>
       <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, p);
   return cudaGetLastError();
 }
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1, bool PML = false>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
+          bool PML = false, bool SEMI = false>
 KernelDesc make_desc() {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
-  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML>,
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
+  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>,
                     C::kThreads,
                     C::kSmemBytes,
                     C::TY,
                     STAGES,
                     C::BW,
                     C::BH,
-                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML>};
+                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>};
 }
 
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `pml`: the wave step
-// that reads eta only in a band along the faces (wave_step_pml).
+// that reads eta only in a band along the faces (wave_step_pml).  `semi`: the sweep with
+// the z stencil split into halves (stencil_apply_semi).
 KernelDesc apply_kernel_desc(int radius);
+KernelDesc semi_kernel_desc(int radius);
 KernelDesc wave_kernel_desc(int radius, bool pml);
 
 }  // namespace libstencil

@@ -14,4 +14,15 @@ KernelDesc apply_kernel_desc(int radius) {
   }
 }
 
+// Semi-stencil sweeps: the ring also keeps the R planes behind the lead (the left half of
+// the z stencil is read from them), so it holds 2R + 1 slots or more.
+KernelDesc semi_kernel_desc(int radius) {
+  switch (radius) {
+    case 1: return make_desc<1, 2, 16, 6, 1, false, 1, 1, false, true>();
+    case 2: return make_desc<2, 2, 16, 7, 1, false, 1, 1, false, true>();
+    case 3: return make_desc<3, 2, 16, 8, 1, false, 1, 1, false, true>();
+    default: return make_desc<4, 2, 16, 9, 1, false, 2, 1, false, true>();
+  }
+}
+
 }  // namespace libstencil

@@ -67,10 +67,10 @@ struct stencil_plan {
   float c[STENCIL_MAX_RADIUS + 1];
   int device;
   int num_sms;
-  KernelDesc kd[3];    // [0] apply, [1] wave, [2] wave with eta in a face band
-  int occupancy[3];    // CTAs per SM
-  StarParams params[3];
-  int grid[3];
+  KernelDesc kd[4];    // [0] apply, [1] wave, [2] wave with eta in a face band, [3] semi apply
+  int occupancy[4];    // CTAs per SM
+  StarParams params[4];
+  int grid[4];
   unsigned* d_status;  // 4 words
   MapEntry maps[kMapCache];
   uint64_t clock;
@@ -133,7 +133,7 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
       best_n = n;
     }
   }
-  if (kind == 0 && R <= 2) {
+  if ((kind == 0 || kind == 3) && R <= 2) {
     // Light sweeps are bound by memory traffic, not by the busiest SM: the fewest chunks
     // that still give every SM a CTA keep the fewest z-fronts in flight and the fewest
     // refilled planes (measured at 512^3, R = 1: 2 chunks 5.7 TB/s, 7 chunks 4.9 TB/s).
@@ -213,7 +213,7 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   return STENCIL_OK;
 }
 
-// Launch one sweep (kind 0) or wave step (1, 2).  nzi >= 0 restricts it to the output
+// Launch one sweep (kind 0, 3) or wave step (1, 2).  nzi >= 0 restricts it to the output
 // planes [R + zoff, R + zoff + nzi).
 int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
            const float* eta, float* out, cudaStream_t stream, int pml = 1 << 30, int zoff = 0,
@@ -226,7 +226,7 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   const CUtensorMap *mu, *mp = nullptr, *mv = nullptr, *me = nullptr;
   int rc = get_map(p, u, kd.box_w, kd.box_h, &mu);
   if (rc) return rc;
-  if (kind >= 1) {
+  if (kind == 1 || kind == 2) {
     if ((rc = get_map(p, uprev, kTX, kd.tile_y, &mp))) return rc;
     if ((rc = get_map(p, v2dt2, kTX, kd.tile_y, &mv))) return rc;
     if ((rc = get_map(p, eta, kTX, kd.tile_y, &me))) return rc;
@@ -401,7 +401,8 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
   p->kd[0] = apply_kernel_desc(radius);
   p->kd[1] = wave_kernel_desc(radius, false);
   p->kd[2] = wave_kernel_desc(radius, true);
-  for (int k = 0; k < 3; ++k) {
+  p->kd[3] = semi_kernel_desc(radius);
+  for (int k = 0; k < 4; ++k) {
     e = cudaFuncSetAttribute(p->kd[k].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->kd[k].smem);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p->occupancy[k], p->kd[k].fn,
@@ -436,6 +437,15 @@ int stencil_apply(stencil_plan* p, const float* in, float* out, void* stream) {
   if ((rc = check_field(p, in, "in")) || (rc = check_field(p, out, "out"))) return rc;
   if (overlap(in, out, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
   return launch(p, 0, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_apply_semi(stencil_plan* p, const float* in, float* out, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, in, "in")) || (rc = check_field(p, out, "out"))) return rc;
+  if (overlap(in, out, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
+  return launch(p, 3, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
 }
 
 int wave_step(stencil_plan* p, const float* u_prev, const float* u, float* u_next,
@@ -613,7 +623,7 @@ int wave_run_host(stencil_plan* p, float* u_prev_host, float* u_host, const floa
 }
 
 int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int n) {
-  if (!p || !info || n < 0 || kind < 0 || kind > 2) return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (!p || !info || n < 0 || kind < 0 || kind > 3) return fail(STENCIL_ERR_ARG, "bad arguments");
   const KernelDesc& kd = p->kd[kind];
   const StarParams& sp = p->params[kind];
   const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.ntiles,

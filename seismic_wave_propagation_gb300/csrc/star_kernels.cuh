@@ -67,7 +67,7 @@ struct Cursor {
   int item, j, L, x0, y0, za, issued, pad;
 };
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, bool SEMI = false>
 struct StarCfg {
   static constexpr int kThreads = kThreadsX * NWY;
   static constexpr int TY = TYT * NWY;  // output tile height
@@ -82,7 +82,7 @@ struct StarCfg {
   static constexpr int kRingOffset = (kCurOff + 2 * (int)sizeof(Cursor) + 127) / 128 * 128;
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
   static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
-  static constexpr int KEEP = WAVE ? R : 0;             // planes kept behind the lead
+  static constexpr int KEEP = (WAVE || SEMI) ? R : 0;   // planes kept behind the lead
   static constexpr int kLookahead = STAGES - KEEP - 1;  // planes in flight beyond the lead
   static_assert(kLookahead >= 1, "ring must hold the kept planes plus one in flight");
   static_assert(BW <= 256 && BH <= 256, "TMA box dimensions are limited to 256");
@@ -236,13 +236,15 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 
 // ---- the kernel ----------------------------------------------------------------------
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML,
+          bool SEMI>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
                       const __grid_constant__ CUtensorMap tm_v2dt2,
                       const __grid_constant__ CUtensorMap tm_eta, const __grid_constant__ StarParams p) {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE>;
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
+  static_assert(!(WAVE && SEMI), "the semi-stencil form is a plain sweep");
   constexpr int TY = C::TY;
   constexpr int BW = C::BW;
   constexpr int KEEP = C::KEEP;
@@ -327,10 +329,12 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     failed = true;
   };
 
-  // s[i][k]: partial sum of the output (i + 1 - R) planes after the current one, row k.
-  P4 s[2 * R][TYT];
+  // s[i][k]: partial sum of the output (i + 1 - R) planes after the current one, row k
+  // (semi-stencil form: of the output R - 1 - i planes before the current one).
+  constexpr int NS = SEMI ? R : 2 * R;
+  P4 s[NS][TYT];
 #pragma unroll
-  for (int i = 0; i < 2 * R; ++i)
+  for (int i = 0; i < NS; ++i)
 #pragma unroll
     for (int k = 0; k < TYT; ++k) s[i][k] = P4{make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   float2 cc[R + 1];  // coefficients duplicated into register pairs
@@ -421,12 +425,37 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         }
       }
 
+      if constexpr (SEMI) {
+        // Semi-stencil form, right half of the z stencil: the landed plane is the last
+        // point of its R predecessors' windows; each partial sum moves one slot down.
+#pragma unroll
+        for (int i = 1; i < R; ++i)
+#pragma unroll
+          for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma2x(cc[R - i], xv[k], s[i][k]);
+      }
+
       if (j >= R && j < L - R) {
         // In-plane part of the landed plane's outputs.  Before the z filter below runs,
         // s[R] holds that plane's partial sums; the filter's FMA then carries them on
         // (they emerge R planes later).  Doing this part first measured 7 % faster than
         // after the filter: the loads issue earlier and the FMA chains overlap better.
-        P4* acc = s[R];
+        // In the semi-stencil form the landed plane's outputs start in the freed slot
+        // s[R-1] with the centre and the left half of the z stencil, read from the R
+        // planes the ring keeps behind the lead.
+        P4* acc = s[SEMI ? R - 1 : R];
+        if constexpr (SEMI) {
+#pragma unroll
+          for (int k = 0; k < TYT; ++k)
+            acc[k] = P4{__fmul2_rn(cc[0], xv[k].a), __fmul2_rn(cc[0], xv[k].b)};
+#pragma unroll
+          for (int r = 1; r <= R; ++r) {
+            int ps = slot - r;
+            if (ps < 0) ps += STAGES;
+            const float* q = ring + ps * PSTRIDE + own;
+#pragma unroll
+            for (int k = 0; k < TYT; ++k) acc[k] = fma2x(cc[r], ldp4(q + k * BW), acc[k]);
+          }
+        }
 #pragma unroll
         for (int k = 0; k < TYT; ++k) {
           const float* rowp = pl + own + k * BW;
@@ -458,7 +487,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
             } else {  // odd distance: pairs straddle registers, scalar
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                pset(acc[k], e, fmaf(p.c[r], X(4 + e - r) + X(4 + e + r), pget(acc[k], e)));
+                pset(acc[k], e, fmaf(cc[r].x, X(4 + e - r) + X(4 + e + r), pget(acc[k], e)));
             }
           }
         }
@@ -476,14 +505,17 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         }
       }
 
-      // z filter, transposed form: every partial sum moves one slot down.
+      if constexpr (!SEMI) {
+        // z filter, transposed form: every partial sum moves one slot down.
 #pragma unroll
-      for (int i = 1; i < 2 * R; ++i)
+        for (int i = 1; i < 2 * R; ++i)
 #pragma unroll
-        for (int k = 0; k < TYT; ++k) s[i - 1][k] = fma2x(cc[i < R ? R - i : i - R], xv[k], s[i][k]);
+          for (int k = 0; k < TYT; ++k)
+            s[i - 1][k] = fma2x(cc[i < R ? R - i : i - R], xv[k], s[i][k]);
 #pragma unroll
-      for (int k = 0; k < TYT; ++k)
-        s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
+        for (int k = 0; k < TYT; ++k)
+          s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
+      }
 
       // Close the step.  Every KB planes (and at the end of an item) the CTA meets at a
       // barrier: every thread is then done with the slots of planes (landed - KEEP) of the
