@@ -152,6 +152,37 @@ def test_star25_1536x1536x256_fifty_sweeps():
           f"final finite fraction {np.isfinite(final).mean():.4f}")
 
 
+def test_star25_1536x1536x256_sweep_time_is_value_independent():
+    """The 50-sweep run overflows to inf and then NaN; the sweep time must not change with
+    the values (no slow path for non-finite or subnormal operands): the median time of
+    sweeps 1-30 (finite) against that of sweeps 35-50 (inf / NaN)."""
+    torch = torch_cuda()
+    nx, ny, nz, R = 1536, 1536, 256, 4
+    u0 = synth.sinusoid_field(nx, ny, nz)
+    plan = StencilPlan(nx, ny, nz, R, synth.laplacian8_coeffs())
+    a = torch.from_numpy(u0.ravel()).cuda()
+    b = a.clone()
+    del u0
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    finite = []
+    for k in range(50):
+        if k in (30, 34):
+            finite.append((k, bool(torch.isfinite(a).all())))
+        ev[k][0].record(s)
+        plan.apply(a, b, s)
+        ev[k][1].record(s)
+        a, b = b, a
+    plan.status(s)
+    ms = [x.elapsed_time(y) for x, y in ev]
+    early, late = float(np.median(ms[0:30])), float(np.median(ms[34:50]))
+    print(f"star25 1536x1536x256: median ms per sweep, sweeps 1-30 {early:.4f}, 35-50 {late:.4f}; "
+          f"input finite at sweeps {finite}")
+    assert finite == [(30, True), (34, False)]  # the late sweeps really run on inf / NaN
+    assert 0.9 < late / early < 1.1
+    plan.close()
+
+
 def test_host_buffer_entry_matches_device_path():
     torch = torch_cuda()
     nx, ny, nz, R = 136, 75, 41, 4
