@@ -392,13 +392,14 @@ def run_profile_case(kind: str):
     import torch
     from seismic_wave_propagation_gb300 import StencilPlan
     n = NX
-    c = synth.laplacian8_coeffs()
-    plan = StencilPlan(n, n, n, R, c)
-    if kind in ("sweep", "semi"):
+    r = 1 if kind == "sweep7" else R
+    c = synth.laplacian2_coeffs() if kind == "sweep7" else synth.laplacian8_coeffs()
+    plan = StencilPlan(n, n, n, r, c)
+    if kind in ("sweep", "semi", "sweep7"):
         u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
         o = u.clone()
         for _ in range(3):
-            (plan.apply if kind == "sweep" else plan.apply_semi)(u, o)
+            (plan.apply_semi if kind == "semi" else plan.apply)(u, o)
     else:
         f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(n, n, n)]
         nxt = f[0].clone()
@@ -406,7 +407,7 @@ def run_profile_case(kind: str):
             plan.wave_step(f[0], f[1], nxt, f[2], f[3])
     torch.cuda.synchronize()
     plan.status()
-    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info({"sweep": 0, "wave": 1, "semi": 3}[kind])}))
+    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info({"sweep": 0, "sweep7": 0, "wave": 1, "semi": 3}[kind])}))
 
 
 def _time_loop(fn, steps, warmup, stream):
@@ -522,7 +523,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
-    ap.add_argument("--profile", choices=["sweep", "wave", "semi"], help="run 3 launches of the 512^3 case (ncu driver)")
+    ap.add_argument("--profile", choices=["sweep", "sweep7", "wave", "semi"],
+                    help="run 3 launches of the 512^3 case (ncu driver); sweep7 is the 7-point Laplacian")
     ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
     if args.profile or args.report_configs:
