@@ -337,7 +337,7 @@ def run_ours(args, dist, rank, local, world):
     # The host link bounds this leg: time plain pinned copies of the same bytes in both
     # directions at once (as the pipelined call overlaps them) and report the step's
     # ceiling at that rate.
-    d_in, d_src = torch.empty(h_in.numel(), device=dev), torch.zeros(h_in.numel(), device=dev)
+    d_in, d_src = torch.empty(h_in.numel(), device=dev), torch.empty(h_in.numel(), device=dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def both_ways():
