@@ -119,17 +119,30 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
   sp.nzi = nzi;
   sp.zoff = zoff;
   const int64_t slots = (int64_t)p->num_sms * std::max(1, p->occupancy[kind]);
-  double best = 1e300;
-  int best_n = 1;
-  for (int n = 1; n <= sp.nzi; ++n) {
+  // Cost of n chunks: rounds of the round-robin schedule x steps per item; and the share
+  // of CTA slots the schedule keeps busy (a partly filled last round idles the rest).
+  auto plan_n = [&](int n, double& cost, double& busy) {
     const int64_t items = (int64_t)sp.ntiles * n;
-    if (items > (int64_t)1 << 30) break;
     const int64_t g = std::min<int64_t>(items, slots);
     const int64_t rounds = (items + g - 1) / g;
-    const double steps = (double)((sp.nzi + n - 1) / n) + 0.35 * 2 * R;
-    const double cost = (double)rounds * steps;
-    if (cost < best * (1.0 - 1e-9)) {
-      best = cost;
+    cost = (double)rounds * ((double)((sp.nzi + n - 1) / n) + 0.35 * 2 * R);
+    busy = (double)items / (double)(rounds * g);
+  };
+  const int max_n = (int)std::min<int64_t>(sp.nzi, ((int64_t)1 << 30) / sp.ntiles);
+  double best = 1e300, cost, busy;
+  for (int n = 1; n <= max_n; ++n) {
+    plan_n(n, cost, busy);
+    best = std::min(best, cost);
+  }
+  // Among near-ties (within 0.5 %), take the fullest schedule: at 1536 x 1536 x 256,
+  // R = 4, 1 and 5 chunks cost the same, and 5 (a 95 % full last round instead of 79 %)
+  // measured 5 % faster.
+  int best_n = 1;
+  double best_busy = -1.0;
+  for (int n = 1; n <= max_n; ++n) {
+    plan_n(n, cost, busy);
+    if (cost <= best * 1.005 && busy > best_busy + 1e-12) {
+      best_busy = busy;
       best_n = n;
     }
   }
