@@ -46,28 +46,34 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The files that make up the device code (the kernels and their instantiation tables).
+DEVICE_SOURCES = ("star_kernels.cuh", "kernel_table.h", "kernels_apply.cu", "kernels_wave.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "seismic_wave_propagation_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in DEVICE_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(key: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+def profiled_traffic(key: str, launch: dict | None = None):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
+    source and, for the launch-geometry keys the entry lists, on the geometry of `launch`."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[key]
-        if e.get("kernel_source_hash") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+        if e.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        if launch is not None and any(e["launch"][k] != launch.get(k) for k in e.get("match", ())):
+            return None
+        return float(e["dram_bytes_per_launch"])
     except Exception:
-        pass
-    return None
+        return None
 
 
 class ClockSampler:
@@ -312,7 +318,7 @@ def run_ours(args, dist, rank, local, world):
                 "gpoints_per_s": wint / (wms / 1e3) / 1e9,
                 "roofline": {"bound": "hbm", "achieved": wbytes / (wms / 1e3) / 1e9, "peak": peak,
                              "unit": "GB/s", "frac": wbytes / (wms / 1e3) / 1e9 / peak,
-                             "traffic": profiled_traffic("wave25_640")},
+                             "traffic": profiled_traffic("wave25_640", wplan.launch_info(1))},
                 "launch": wplan.launch_info(1),
                 "pml16": {"ms_per_step": pms, "gpoints_per_s": wint / (pms / 1e3) / 1e9,
                           "wave_step_bytes_over_time_gbs": wbytes / (pms / 1e3) / 1e9}}
@@ -375,7 +381,7 @@ def run_ours(args, dist, rank, local, world):
                            "launch": info},
                 "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": profiled_traffic("star25_512"),
+                             "frac": achieved / peak, "traffic": profiled_traffic("star25_512", info),
                              "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                              else "fallback 6.8 TB/s",
                              "algorithmic_bytes_per_launch": algo_bytes,

@@ -120,13 +120,13 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
   sp.zoff = zoff;
   const int64_t slots = (int64_t)p->num_sms * std::max(1, p->occupancy[kind]);
   // Cost of n chunks: rounds of the round-robin schedule x steps per item; and the share
-  // of CTA slots the schedule keeps busy (a partly filled last round idles the rest).
+  // of the GPU's CTA slots the schedule keeps busy (a partly filled round idles the rest).
   auto plan_n = [&](int n, double& cost, double& busy) {
     const int64_t items = (int64_t)sp.ntiles * n;
     const int64_t g = std::min<int64_t>(items, slots);
     const int64_t rounds = (items + g - 1) / g;
     cost = (double)rounds * ((double)((sp.nzi + n - 1) / n) + 0.35 * 2 * R);
-    busy = (double)items / (double)(rounds * g);
+    busy = (double)items / (double)(rounds * slots);
   };
   const int max_n = (int)std::min<int64_t>(sp.nzi, ((int64_t)1 << 30) / sp.ntiles);
   double best = 1e300, cost, busy;

@@ -73,3 +73,8 @@ def test_json_helpers():
     assert len(h) == 16
     t = bench.profiled_traffic("star25_512")
     assert t is None or t > 1e9
+    # The recorded traffic is reported only for the launch geometry it was captured on.
+    e = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["star25_512"]
+    if t is not None:
+        assert bench.profiled_traffic("star25_512", dict(e["launch"])) == t
+        assert bench.profiled_traffic("star25_512", dict(e["launch"], zchunks=e["launch"]["zchunks"] + 1)) is None
