@@ -23,28 +23,28 @@ struct KernelDesc {
 };
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false>
+          bool PML = false, bool SEMI = false, bool DRIFT = false>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
                         const StarParams& p) {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
-  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>
+  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>
       <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, p);
   return cudaGetLastError();
 }
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false>
+          bool PML = false, bool SEMI = false, bool DRIFT = false>
 KernelDesc make_desc() {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
-  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>,
+  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>,
                     C::kThreads,
                     C::kSmemBytes,
                     C::TY,
                     STAGES,
                     C::BW,
                     C::BH,
-                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI>};
+                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>};
 }
 
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `pml`: the wave step

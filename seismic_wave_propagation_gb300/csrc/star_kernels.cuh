@@ -14,7 +14,10 @@
 //   * Each plane's (64+8) x (TY+2R) box is staged into a shared-memory ring by TMA
 //     (cp.async.bulk.tensor.3d), completion tracked by an mbarrier per slot (expect-tx
 //     bytes).  The CTA meets at one barrier per plane; right after it, lane 0 of one warp
-//     (the duty rotates over the warps) refills the slot the plane just released.
+//     (the duty rotates over the warps) refills the slot the plane just released.  With
+//     DRIFT (plain and semi sweeps) there is no per-plane barrier: each warp counts itself
+//     off a slot in shared memory when done with it, and the last one refills it, so the
+//     warps drift apart by up to the ring's lookahead.
 //     Out-of-range box parts are zero-filled by the TMA unit and only ever feed outputs
 //     that are masked off.
 //   * Every thread owns a 4 x TYT block of output columns (one float4 per row).  Along z
@@ -79,7 +82,9 @@ struct StarCfg {
   static constexpr int kAuxStageBytes = 3 * kAuxFieldBytes;
   static constexpr int kNumBars = STAGES + (WAVE ? ASTAGES : 0);
   static constexpr int kCurOff = (8 * kNumBars + 15) / 16 * 16;
-  static constexpr int kRingOffset = (kCurOff + 2 * (int)sizeof(Cursor) + 127) / 128 * 128;
+  static constexpr int kCntOff = kCurOff + 2 * (int)sizeof(Cursor);  // release counters
+  static constexpr int kIssOff = kCntOff + 4 * kNumBars;                // last load per slot
+  static constexpr int kRingOffset = (kIssOff + 4 * kNumBars + 127) / 128 * 128;
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
   static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
   static constexpr int KEEP = (WAVE || SEMI) ? R : 0;   // planes kept behind the lead
@@ -237,7 +242,7 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 // ---- the kernel ----------------------------------------------------------------------
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML,
-          bool SEMI>
+          bool SEMI, bool DRIFT>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
@@ -245,6 +250,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
                       const __grid_constant__ CUtensorMap tm_eta, const __grid_constant__ StarParams p) {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
   static_assert(!(WAVE && SEMI), "the semi-stencil form is a plain sweep");
+  static_assert(!(WAVE && DRIFT), "the wave step's aux ring needs the per-plane barrier");
   constexpr int TY = C::TY;
   constexpr int BW = C::BW;
   constexpr int KEEP = C::KEEP;
@@ -252,6 +258,8 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 
   extern __shared__ __align__(128) unsigned char smem[];
   Cursor* cur = reinterpret_cast<Cursor*>(smem + C::kCurOff);  // [0] u loads, [1] aux loads
+  int* relcnt = reinterpret_cast<int*>(smem + C::kCntOff);     // warps done with a slot
+  int* lastld = reinterpret_cast<int*>(smem + C::kIssOff);     // last load counter per slot
   const uint32_t base = smem_addr(smem);
   const uint32_t ring_base = base + C::kRingOffset;
   const uint32_t aux_base = base + C::kAuxOffset;
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     if (k.item >= p.nitems) return;
     const int slot = counter % STAGES;
     const uint32_t bar = base + 8u * slot;
+    lastld[slot] = counter;
     if (counter != p.debug_skip) {
       mbar_arrive_expect_tx(bar, C::kPlaneBytes);
       tma_load_3d(ring_base + slot * C::kPlaneStride, &tm_u, bar, k.x0 - kHX, k.y0 - R,
@@ -307,7 +316,11 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   const bool bad_smem = (base & 127u) != 0u;  // TMA destinations need 128-B alignment
   if (leader) {
     if (bad_smem) atomicOr(p.status, kStatusBadSmem);
-    for (int s = 0; s < C::kNumBars; ++s) mbar_init(base + 8u * s, 1);
+    for (int s = 0; s < C::kNumBars; ++s) {
+      mbar_init(base + 8u * s, 1);
+      relcnt[s] = 0;
+      lastld[s] = -1;
+    }
     fence_mbar_init();
     cursor_set_item<R, TY>(p, cur[0], blockIdx.x);
     cur[0].issued = 0;
@@ -517,6 +530,47 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
           s[2 * R - 1][k] = P4{__fmul2_rn(cc[R], xv[k].a), __fmul2_rn(cc[R], xv[k].b)};
       }
 
+      if constexpr (DRIFT) {
+        // Close the step without a CTA barrier: this warp is done with the slot of plane
+        // (landed - KEEP).  The last warp to release it refills it with the plane STAGES
+        // loads later, located from this warp's own progress (no shared cursor).
+        const int rslot = (slot + STAGES - KEEP) % STAGES;
+        ++J;
+        if (++slot == STAGES) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        if (__any_sync(0xffffffffu, failed)) {  // a wait of this warp ran out: leave
+          failed = true;
+          break;
+        }
+        __syncwarp();
+        if (lane0 && atomicAdd(&relcnt[rslot], 1) == NWARPS - 1) {
+          relcnt[rslot] = 0;  // published to the next round by the refill's arrive (release)
+          int jj = j + STAGES - KEEP, it = item, L2 = L, nx0 = x0, ny0 = y0, nza = za;
+          while (jj >= L2 && it < p.nitems) {
+            jj -= L2;
+            it += (int)gridDim.x;
+            if (it < p.nitems) {
+              int zb2;
+              item_geometry<R, TY>(p, it, nx0, ny0, nza, zb2);
+              L2 = zb2 - nza + 2 * R;
+            }
+          }
+          if (it < p.nitems) {
+            const int counter = J - 1 + STAGES - KEEP;
+            const uint32_t bar = base + 8u * rslot;
+            lastld[rslot] = counter;
+            fence_proxy_async_smem();
+            if (counter != p.debug_skip) {
+              mbar_arrive_expect_tx(bar, C::kPlaneBytes);
+              tma_load_3d(ring_base + rslot * C::kPlaneStride, &tm_u, bar, nx0 - kHX, ny0 - R,
+                          nza - R + jj);
+            }
+          }
+        }
+        continue;
+      }
       // Close the step.  Every KB planes (and at the end of an item) the CTA meets at a
       // barrier: every thread is then done with the slots of planes (landed - KEEP) of the
       // steps since the last barrier, and one warp (rotating) refills them.
@@ -545,18 +599,24 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
       if (++pwarp == NWARPS) pwarp = 0;
       if (stop) goto drain;
     }
+    if (DRIFT && failed) break;
+  }
+  if constexpr (DRIFT) {
+    // The warps leave the loops at different times; they meet here to decide together.
+    if (__syncthreads_or(failed)) goto drain;
   }
   return;
 
 drain:
   // A wait ran out: make sure none of this CTA's copies is still landing in shared
   // memory before the CTA exits (bounded as well), then leave.
-  // Only the last STAGES (ASTAGES) loads issued can still be outstanding, one per slot.
+  // Only the last load issued into each slot can still be outstanding.
   if (leader) {
-    const int nu = cur[0].issued;
-    for (int c = nu > STAGES ? nu - STAGES : 0; c < nu; ++c)
-      if (c != p.debug_skip && !mbar_wait_bounded(base + 8u * (c % STAGES), (c / STAGES) & 1))
+    for (int sl = 0; sl < STAGES; ++sl) {
+      const int c = lastld[sl];
+      if (c >= 0 && c != p.debug_skip && !mbar_wait_bounded(base + 8u * sl, (c / STAGES) & 1))
         atomicOr(p.status, kStatusDrainTimeout);
+    }
     if (WAVE) {
       const int na = cur[1].issued;
       for (int c = na > ASTAGES ? na - ASTAGES : 0; c < na; ++c)

@@ -17,11 +17,13 @@ from gpu_util import interior_mask, sweep_tol, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kind", ["apply", "wave"])
-def test_lost_load_times_out_and_plan_recovers(kind):
+@pytest.mark.parametrize("kind,R", [("apply", 4), ("apply", 1), ("semi", 4), ("wave", 4)])
+def test_lost_load_times_out_and_plan_recovers(kind, R):
+    """R = 4 sweeps close each plane with a CTA barrier, R = 1 sweeps release ring slots
+    warp by warp: both protocols must turn a lost load into a timeout."""
     torch = torch_cuda()
-    nx, ny, nz, R = 136, 75, 41, 4
-    c = synth.laplacian8_coeffs()
+    nx, ny, nz = 136, 75, 41
+    c = synth.laplacian8_coeffs() if R == 4 else synth.laplacian2_coeffs()
     plan = StencilPlan(nx, ny, nz, R, c)
     u = synth.uniform_field(nx, ny, nz)
     d = torch.from_numpy(u.ravel()).cuda()
@@ -31,6 +33,8 @@ def test_lost_load_times_out_and_plan_recovers(kind):
     def run():
         if kind == "apply":
             plan.apply(d, out)
+        elif kind == "semi":
+            plan.apply_semi(d, out)
         else:
             plan.wave_step(aux[1], d, out, aux[0], aux[1])
 
@@ -44,7 +48,7 @@ def test_lost_load_times_out_and_plan_recovers(kind):
     plan.debug_inject(0)
     run()
     plan.status(None, d)  # status was cleared by the previous read; this run is clean
-    if kind == "apply":
+    if kind in ("apply", "semi"):
         m = interior_mask(u.shape, R)
         want = oracle.apply(u, c.astype(np.float32), R)
         got = out.cpu().numpy().reshape(u.shape)
