@@ -69,6 +69,22 @@ def test_empty_interior_is_noop():
     assert np.all(out.view(np.uint32) == 0x7FC0DEAD)
 
 
+@pytest.mark.parametrize("nx,ny,nz,R", [(1024, 1024, 20, 1), (2048, 512, 24, 2), (1024, 1024, 30, 3)])
+def test_several_items_per_cta(nx, ny, nz, R):
+    """More work items than resident CTAs: each CTA streams several tiles in turn, and the
+    ring's refills run from one item into the next (the radii 1-3 release slots warp by
+    warp and locate each refill themselves)."""
+    torch = torch_cuda()
+    u = synth.uniform_field(nx, ny, nz, seed=3000 + R)
+    c = np.random.default_rng(20 + R).uniform(-1, 1, R + 1)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    info = plan.launch_info(0)
+    assert info["tiles"] * info["zchunks"] > info["grid"], info  # several items per CTA
+    plan.close()
+    out = run_apply(torch, u, c, R)
+    check(u, out, c, R)
+
+
 def test_star7_avg_64_shell_copied():
     """7-point smoothing on 64^3 with the shell copied from the input."""
     torch = torch_cuda()
