@@ -1,7 +1,8 @@
 // Stencil-sweep kernel instantiations, radius 1..4.
 // Tile 64 x 32 outputs, 256 threads (4 x 2 outputs per thread).  Only the lead plane is
-// read from shared memory, so the ring is the landed plane plus R+3 in flight (R = 4: 5;
-// 5 to 6 slots measured 2 % faster than 7 or 8 at 512^3, two CTAs per SM either way).
+// read from shared memory, so the ring is the landed plane plus R+3 in flight (radius 4:
+// a 5-slot ring and one CTA barrier per 2 planes, 1-3 % faster than a barrier per plane on
+// eight of nine grid shapes from 384^3 to 2048 x 512 x 512; 7 or 8 slots are slower).
 // Radii 1-3 release ring slots warp by warp (DRIFT; at 512^3 2-6 % faster than a CTA
 // barrier per plane), radius 4 keeps the barrier (1-2 % faster there).
 #include "kernel_table.h"
@@ -13,7 +14,7 @@ KernelDesc apply_kernel_desc(int radius) {
     case 1: return make_desc<1, 2, 16, 5, 1, false, 1, 1, false, false, true>();
     case 2: return make_desc<2, 2, 16, 6, 1, false, 1, 1, false, false, true>();
     case 3: return make_desc<3, 2, 16, 7, 1, false, 1, 1, false, false, true>();
-    default: return make_desc<4, 2, 16, 6, 1, false, 2>();
+    default: return make_desc<4, 2, 16, 5, 1, false, 2, 2>();
   }
 }
 
