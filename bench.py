@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -51,11 +52,16 @@ DEVICE_SOURCES = ("star_kernels.cuh", "kernel_table.h", "kernels_apply.cu", "ker
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device code with comments and whitespace removed (the sources hold no
+    string literal with a comment marker), so that comment edits keep recorded counters."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "seismic_wave_propagation_gb300", "csrc")
     for name in DEVICE_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

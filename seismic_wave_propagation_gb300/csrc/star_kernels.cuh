@@ -13,9 +13,9 @@
 //     at the same time and their halos are served from L2.
 //   * Each plane's (64+8) x (TY+2R) box is staged into a shared-memory ring by TMA
 //     (cp.async.bulk.tensor.3d), completion tracked by an mbarrier per slot (expect-tx
-//     bytes).  The CTA meets at one barrier per plane; right after it, lane 0 of one warp
-//     (the duty rotates over the warps) refills the slot the plane just released.  With
-//     DRIFT (plain and semi sweeps) there is no per-plane barrier: each warp counts itself
+//     bytes).  The CTA meets at one barrier every KB planes; right after it, lane 0 of one
+//     warp (the duty rotates over the warps) refills the slots released since the last
+//     one.  With DRIFT (sweeps of radius 1-3) there is no barrier: each warp counts itself
 //     off a slot in shared memory when done with it, and the last one refills it, so the
 //     warps drift apart by up to the ring's lookahead.
 //     Out-of-range box parts are zero-filled by the TMA unit and only ever feed outputs
@@ -28,7 +28,9 @@
 //     one slot down, so the z window needs no register moves and no unrolling.  The
 //     in-plane part of plane p's outputs (x and y neighbours, read from the landed box)
 //     is added to s_R, which emerges R planes later.  The stencil sweep therefore needs
-//     only the lead plane in shared memory; the wave step keeps R more planes for u(z).
+//     only the lead plane in shared memory; the wave step keeps R more planes for u(z),
+//     and so does the semi-stencil form (SEMI), which reads the centre and one half of
+//     the z stencil from those planes and carries the other half in R partial sums.
 //   * Every wait on an mbarrier is bounded (about 2 s).  When it runs out the kernel
 //     records an error in the status block, waits (bounded) for its own copies still in
 //     flight and returns; the host reads the status.
