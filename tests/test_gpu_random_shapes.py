@@ -1,0 +1,75 @@
+"""Seeded random grid shapes against the oracle: every radius, both ring protocols (radius 4
+meets at a CTA barrier, radii 1-3 release slots warp by warp), the semi-stencil sweep and
+the wave step, on sizes that are ragged in every axis (partial x and y tiles, short and
+uneven z-chunks, empty interiors)."""
+import numpy as np
+import pytest
+
+import oracle
+from seismic_wave_propagation_gb300 import StencilPlan, synth
+from gpu_util import Guarded, interior_mask, sweep_tol, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def shapes(seed: int, count: int):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        R = int(rng.integers(1, 5))
+        nx = 4 * int(rng.integers(1, 80))  # 4 .. 316, x rows stay 16-byte aligned
+        ny = int(rng.integers(1, 140))
+        nz = int(rng.integers(1, 70))
+        out.append((nx, ny, nz, R))
+    return out
+
+
+SWEEP_SHAPES = shapes(2024, 24)
+WAVE_SHAPES = shapes(2025, 10)
+
+
+@pytest.mark.parametrize("semi", [False, True])
+@pytest.mark.parametrize("nx,ny,nz,R", SWEEP_SHAPES)
+def test_random_shape_sweep(nx, ny, nz, R, semi):
+    torch = torch_cuda()
+    u = synth.uniform_field(nx, ny, nz, seed=nx * 7 + ny * 11 + nz * 13 + R)
+    c = np.random.default_rng(nx + ny + nz).uniform(-1, 1, R + 1)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    gin = Guarded(torch, u)
+    gout = Guarded(torch, u, fill_sentinel=True)
+    (plan.apply_semi if semi else plan.apply)(gin.ptr, gout.ptr)
+    plan.status()
+    got = gout.numpy()
+    assert gin.guards_intact() and gout.guards_intact()
+    plan.close()
+    c32 = np.asarray(c, np.float32)
+    m = interior_mask(u.shape, R)
+    want = oracle.apply(u, c32, R, out=np.zeros_like(u))
+    if m.any():
+        assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= sweep_tol(c32, u)
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD), "shell written"
+
+
+@pytest.mark.parametrize("nx,ny,nz,R", WAVE_SHAPES)
+def test_random_shape_wave_step(nx, ny, nz, R):
+    torch = torch_cuda()
+    seed = nx + 3 * ny + 5 * nz + R
+    up = synth.uniform_field(nx, ny, nz, seed=seed)
+    u = synth.uniform_field(nx, ny, nz, seed=seed + 1)
+    s = synth.uniform_field(nx, ny, nz, seed=seed + 2, scale=0.1) + np.float32(0.1)
+    e = synth.sponge_eta(nx, ny, nz, width=6)
+    c = np.random.default_rng(seed).uniform(-0.3, 0.3, R + 1)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    gs = [Guarded(torch, a) for a in (up, u, s, e)]
+    gn = Guarded(torch, u, fill_sentinel=True)
+    plan.wave_step(gs[0].ptr, gs[1].ptr, gn.ptr, gs[2].ptr, gs[3].ptr)
+    plan.status()
+    got = gn.numpy()
+    assert all(g.guards_intact() for g in gs + [gn])
+    plan.close()
+    want = oracle.wave_step(up, u, s, e, np.asarray(c, np.float32), R, u_next=np.zeros_like(u))
+    m = interior_mask(u.shape, R)
+    if m.any():
+        tol = 1e-5 * (2 + 0.2 * float(np.sum(np.abs(c)))) * 2.0
+        assert np.max(np.abs(got[m] - want[m])) <= tol
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD)
