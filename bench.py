@@ -422,10 +422,17 @@ def run_profile_case(kind: str):
     print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info({"sweep": 0, "sweep7": 0, "wave": 1, "semi": 3}[kind])}))
 
 
-def _time_loop(fn, steps, warmup, stream):
+def _time_loop(fn, steps, warmup, stream, warm_seconds=0.3):
+    """Mean CUDA-event time of `fn` over `steps` calls, after at least `warmup` calls and at
+    least `warm_seconds` of warm-up (the GPU may have idled through CPU work before)."""
     import torch
-    for _ in range(warmup):
+    t0 = time.perf_counter()
+    done = 0
+    while done < warmup or time.perf_counter() - t0 < warm_seconds:
         fn()
+        done += 1
+        if done % 8 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -434,6 +441,39 @@ def _time_loop(fn, steps, warmup, stream):
     b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps
+
+
+def _first_step_parity(torch, plan, w, c, stream, samples=40000):
+    """The workload's first sweep or step from its initial fields, checked against the
+    oracle at sampled interior points: the largest error as a fraction of the tolerance
+    (1e-5 * sum|c| * max|u| per sweep; 2e-5 * (2 + 0.2 * sum|c|) * max|u| for a step)."""
+    import oracle
+    oracle.build()
+    nx, ny, nz, r = w["nx"], w["ny"], w["nz"], w["radius"]
+    rng = np.random.default_rng(11)
+    idx = (rng.integers(r, nx - r, samples) + nx * (rng.integers(r, ny - r, samples)
+                                                  + ny * rng.integers(r, nz - r, samples))).astype(np.int64)
+    c32 = c.astype(np.float32)
+    with torch.cuda.stream(stream):
+        if w["init"] == "wave":
+            f = synth.wave_fields(nx, ny, nz)
+            d = [torch.from_numpy(a.ravel()).cuda() for a in f]
+            nxt = d[0].clone()
+            plan.wave_step(d[0], d[1], nxt, d[2], d[3], stream)
+            plan.status(stream)
+            got = nxt.cpu().numpy()[idx]
+            want = oracle.wave_points(f[0], f[1], f[2], f[3], c32, r, idx)
+            tol = 2e-5 * (2 + 0.2 * float(np.sum(np.abs(c32)))) * float(np.max(np.abs(f[1])))
+        else:
+            u0 = synth.sinusoid_field(nx, ny, nz) if w["init"] == "sinusoids" else synth.uniform_field(nx, ny, nz)
+            d = torch.from_numpy(u0.ravel()).cuda()
+            o = d.clone()
+            plan.apply(d, o, stream)
+            plan.status(stream)
+            got = o.cpu().numpy()[idx]
+            want = oracle.apply_points(u0, c32, r, idx)
+            tol = 1e-5 * float(np.sum(np.abs(c32))) * float(np.max(np.abs(u0)))
+    return float(np.max(np.abs(got.astype(np.float64) - want))) / tol
 
 
 def run_report_configs(args):
@@ -470,11 +510,16 @@ def run_report_configs(args):
             reps = max(1, min(101, int(2000 // max(1, units))))
             ms = _time_loop(loop, reps, 3, stream)
             plan.status(stream)
+            parity = None if args.skip_cpu else _first_step_parity(torch, plan, w, c, stream)
         ms_unit = ms / units
+        key = {"star25_lap8_512": ("star25_512", 0), "wave25_640": ("wave25_640", 1)}.get(name)
+        dram = profiled_traffic(key[0], plan.launch_info(key[1])) if key else None
         line = {"workload": name, "grid": [nx, ny, nz], "radius": r, "units": units,
                 "ms_per_sweep_or_step": ms_unit, "gpoints_per_s": interior / (ms_unit / 1e3) / 1e9,
                 "hbm_gbs": per / (ms_unit / 1e3) / 1e9, "frac_of_peak": per / (ms_unit / 1e3) / 1e9 / peak,
-                "timed_loops": reps}
+                "compulsory_bytes_per_point": per / interior,
+                "dram_bytes_per_point_ncu": dram / interior if dram else None,
+                "parity_max_err_over_tol": parity, "timed_loops": reps}
         if not args.skip_cpu:
             import oracle
             oracle.build()
@@ -514,11 +559,15 @@ def run_report_configs(args):
         print(json.dumps(row), flush=True)
         cmp.append(row)
         plan.close()
-    print("| workload | GPoints/s | HBM GB/s | % of measured peak | ms per sweep/step | CPU oracle GPoints/s |")
-    print("|---|---|---|---|---|---|")
+    print("| workload | GPoints/s | HBM GB/s | % of measured peak | ms per sweep/step | B/pt DRAM (ncu) / compulsory "
+          "| parity max err/tol | CPU oracle GPoints/s |")
+    print("|---|---|---|---|---|---|---|---|")
     for l in out:
+        dram = "—" if l["dram_bytes_per_point_ncu"] is None else f"{l['dram_bytes_per_point_ncu']:.2f}"
+        par = "—" if l["parity_max_err_over_tol"] is None else f"{l['parity_max_err_over_tol']:.3f}"
         print(f"| {l['workload']} | {l['gpoints_per_s']:.1f} | {l['hbm_gbs']:.0f} | {100 * l['frac_of_peak']:.1f} | "
-              f"{l['ms_per_sweep_or_step']:.4f} | {l.get('cpu_oracle_gpoints_per_s', float('nan')):.2f} |")
+              f"{l['ms_per_sweep_or_step']:.4f} | {dram} / {l['compulsory_bytes_per_point']:.2f} | {par} | "
+              f"{l.get('cpu_oracle_gpoints_per_s', float('nan')):.2f} |")
     print("| sweep kernel | transposed z filter: ms, % of peak | semi-stencil: ms, % of peak |")
     print("|---|---|---|")
     for row in cmp:
