@@ -36,6 +36,8 @@ NX = NY = NZ = 512
 R = 4
 WAVE_N = 640
 FALLBACK_HBM_GBS = 6800.0
+E2E_WARMUP = 3
+E2E_CALLS = 20
 
 
 def peaks():
@@ -196,6 +198,13 @@ def time_oracle(u: np.ndarray, c: np.ndarray, budget_s: float, min_reps: int = 1
     return pts * reps / t, sample, oracle.num_threads()
 
 
+def bench_config(world: int) -> dict:
+    """The workload both arms time (the GPU line and the reference arm print this same dict)."""
+    return {"workload": "star25_lap8_512", "nx": NX, "ny": NY, "nz": NZ, "radius": R,
+            "coeffs": "8th-order Laplacian, h=1", "l2": "inputs (512 MiB) larger than L2; no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, dist, rank, world):
     """Reference arm: the CPU oracle as it stands, on the host cores, same metric/config."""
     if rank != 0:
@@ -219,8 +228,7 @@ def run_reference(args, dist, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "star25_lap8_512", "nx": NX, "ny": NY, "nz": NZ, "radius": R,
-                       "parallelism": "replicas"},
+            "config": bench_config(world),
             "cpu_baseline": {"value": gpts, "unit": "GPoints/s", "cores": cores, "kind": "oracle",
                              "sample": samples[-1] if samples else ""},
             "e2e": {"value": gpts, "unit": "GPoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -276,8 +284,68 @@ def run_ours(args, dist, rank, local, world):
     achieved = algo_bytes / avg_launch_s / 1e9
     clocks = clk.summary()
 
+    # ---- end to end through the host-buffer C-ABI call --------------------------------
+    # Every call copies the step's input in from pinned host memory and its result out
+    # (1 GiB of host transfers), pipelined over z-slabs inside the library.  Median of
+    # E2E_CALLS timed calls after E2E_WARMUP untimed ones.
+    h_in = torch.from_numpy(u.ravel()).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    in_np, out_np = h_in.numpy(), h_out.numpy()
+    for _ in range(E2E_WARMUP):
+        plan.apply_host(in_np, out_np, 1, s)
+    torch.cuda.synchronize(dev)
+    e2e_times, phases = [], []
+    for _ in range(E2E_CALLS):
+        t0 = time.perf_counter()
+        plan.apply_host(in_np, out_np, 1, s)
+        e2e_times.append(time.perf_counter() - t0)
+        phases.append(plan.host_phases())
+    e2e_s = statistics.median(e2e_times)
+    e2e_s = max_over_ranks(dist, e2e_s)
+    mid = sorted(range(len(e2e_times)), key=lambda i: e2e_times[i])[len(e2e_times) // 2]
+    e2e = {"value": sum_over_ranks(dist, float(interior)) / e2e_s / 1e9, "unit": "GPoints/s",
+           "h2d_bytes_per_step": 4 * NX * NY * NZ, "d2h_bytes_per_step": 4 * NX * NY * NZ,
+           "ms_per_step": e2e_s * 1e3, "steps": E2E_CALLS, "warmup": E2E_WARMUP,
+           "ms_min": min(e2e_times) * 1e3, "ms_max": max(e2e_times) * 1e3,
+           "phases_of_median_call": phases[mid]}
+    # The host link bounds this leg: time plain pinned copies of the same bytes, one way
+    # at a time and both ways at once (as the pipelined call overlaps them), and report
+    # the step's ceiling at the both-ways rate.
+    d_in, d_src = torch.empty(h_in.numel(), device=dev), torch.empty(h_in.numel(), device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            h_out.copy_(d_src, non_blocking=True)
+
+    def both_ways():
+        h2d()
+        d2h()
+
+    def median_s(fn, n=7):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts)
+    link_s = median_s(both_ways)
+    nbytes = 4 * NX * NY * NZ
+    e2e["link"] = {"each_way_gbs": nbytes / link_s / 1e9, "ms": link_s * 1e3,
+                   "h2d_alone_gbs": nbytes / median_s(h2d) / 1e9, "d2h_alone_gbs": nbytes / median_s(d2h) / 1e9,
+                   "ceiling_value": float(interior) / link_s / 1e9,
+                   "frac": (float(interior) / e2e_s) / (float(interior) / link_s),
+                   "how": "pinned cudaMemcpyAsync of the step's bytes, H2D and D2H on two streams at once (median of 7)"}
+    del d_in, d_src, h_in, h_out
+
     # ---- fused wave step at 640^3 ----------------------------------------------------
-    del d_out
     wave = None
     if not args.skip_wave:
         n = WAVE_N
@@ -325,45 +393,6 @@ def run_ours(args, dist, rank, local, world):
                           "wave_step_bytes_over_time_gbs": wbytes / (pms / 1e3) / 1e9}}
         wplan.close()
         del f, nxt, a, b
-
-    # ---- end to end through the host-buffer C-ABI call --------------------------------
-    h_in = torch.from_numpy(u.ravel()).pin_memory()
-    h_out = torch.empty_like(h_in).pin_memory()
-    in_np, out_np = h_in.numpy(), h_out.numpy()
-    plan.apply_host(in_np, out_np, 1, s)
-    e2e_steps = max(3, min(20, args.steps // 100))
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        plan.apply_host(in_np, out_np, 1, s)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_s = max_over_ranks(dist, e2e_s)
-    e2e = {"value": sum_over_ranks(dist, float(interior)) / e2e_s / 1e9, "unit": "GPoints/s",
-           "h2d_bytes_per_step": 4 * NX * NY * NZ, "d2h_bytes_per_step": 4 * NX * NY * NZ,
-           "ms_per_step": e2e_s * 1e3, "steps": e2e_steps}
-    # The host link bounds this leg: time plain pinned copies of the same bytes in both
-    # directions at once (as the pipelined call overlaps them) and report the step's
-    # ceiling at that rate.
-    d_in, d_src = torch.empty(h_in.numel(), device=dev), torch.empty(h_in.numel(), device=dev)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-
-    def both_ways():
-        with torch.cuda.stream(s_in):
-            d_in.copy_(h_in, non_blocking=True)
-        with torch.cuda.stream(s_out):
-            h_out.copy_(d_src, non_blocking=True)
-    both_ways()
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(5):
-        both_ways()
-    torch.cuda.synchronize(dev)
-    link_s = (time.perf_counter() - t0) / 5
-    e2e["link"] = {"each_way_gbs": 4 * NX * NY * NZ / link_s / 1e9, "ms": link_s * 1e3,
-                   "ceiling_value": float(interior) / link_s / 1e9,
-                   "frac": (float(interior) / e2e_s) / (float(interior) / link_s),
-                   "how": "pinned cudaMemcpyAsync of the step's bytes, H2D and D2H on two streams at once"}
-    del d_in, d_src
     plan.close()
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ---------------------------------------
@@ -376,10 +405,7 @@ def run_ours(args, dist, rank, local, world):
         line = {"metric": METRIC, "value": gpts, "unit": "GPoints/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": "star25_lap8_512", "nx": NX, "ny": NY, "nz": NZ, "radius": R,
-                           "coeffs": "8th-order Laplacian, h=1", "l2": "inputs (512 MiB) larger than L2; no flush",
-                           "parallelism": "replicas" if world > 1 else "single GPU",
-                           "launch": info},
+                "config": bench_config(world), "launch": info,
                 "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": profiled_traffic("star25_512", info),

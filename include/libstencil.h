@@ -179,6 +179,29 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
 int stencil_plan_launch_info(const stencil_plan* plan, int kind, int64_t* info, int n);
 
 /*
+ * Where the time of the plan's last pipelined host-buffer sweep (stencil_apply_host with
+ * nsweeps == 1) went, from CUDA events on its three streams, in milliseconds since the
+ * call's start: ms[0] the whole call (last copy out done), ms[1] the first slab landed on
+ * the device, ms[2] the last slab landed (copies in done), ms[3] the last slab swept;
+ * ms[4] is the number of slabs.  Valid after that call returned; n values at most 5 are
+ * written.  Returns the number written, or STENCIL_ERR_ARG if no such call has run.
+ */
+int stencil_plan_host_phases(const stencil_plan* plan, float* ms, int n);
+
+/*
+ * The z-chunk schedule stencil_plan_create would choose for `kind` (as for
+ * stencil_plan_launch_info) on a GPU with `num_sms` SMs that holds `ctas_per_sm` CTAs of
+ * that kernel per SM.  Host-only: makes no CUDA call, so it also runs without a GPU
+ * (capacity planning, tests).  Its cost does not grow with nz.  Writes to info[0..n):
+ * grid CTAs, x-y tiles, z-chunks per tile column, work items, tile width, tile height
+ * (all 0 but the tile sizes when the interior is empty).  Returns the number of values
+ * written, or STENCIL_ERR_ARG for a grid or radius stencil_plan_create would reject, a
+ * kind outside [0, 3], num_sms or ctas_per_sm < 1.
+ */
+int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int kind,
+                           int num_sms, int ctas_per_sm, int64_t* info, int n);
+
+/*
  * Test hook for the device watchdog: mode 1 makes every CTA of the plan's next launches
  * skip one of its staged loads, so the bounded wait for it runs out and
  * stencil_plan_status returns STENCIL_ERR_TIMEOUT; mode 0 restores normal operation.
@@ -197,12 +220,15 @@ int stencil_debug_inject(stencil_plan* plan, int mode);
  * Scratch: the kernel's 16-byte status block lives in a file-scope device array of 256
  * bytes that every GPU which loads the library holds until the process exits.  The need
  * does not grow with the grid; grids beyond the library's maximum (each dimension
- * <= 2^30, at most 2^40 points) are rejected with STENCIL_ERR_ARG.  The first call on a
- * device looks up the array's device address (once per device, that device current);
- * make that first call before any stream capture.  The call clears the status words,
- * enqueues the sweep on `stream`, then synchronises `stream` so that it can report a
- * device-side timeout (STENCIL_ERR_TIMEOUT).  Every call shares the one array per device:
- * calls that overlap on the GPU (other host threads, other streams) race on it.
+ * <= 2^30, at most 2^40 points) are rejected with STENCIL_ERR_ARG.  Every call looks up
+ * the array's address in the current device's context (cudaGetSymbolAddress, which
+ * allocates nothing); the first lookup in a context may load the library's device code
+ * there, so make the first call on a device before any stream capture.  The call clears
+ * the status words, enqueues the sweep on `stream`, then synchronises `stream` so that it
+ * can report a device-side timeout (STENCIL_ERR_TIMEOUT); it must therefore not be made
+ * from a CUDA stream callback or host function, where CUDA forbids those calls.  Every
+ * call shares the one array per device: calls that overlap on the GPU (other host
+ * threads, other streams) race on it.
  */
 int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int radius, const float* coeffs,
                           const float* in, float* out, void* stream);

@@ -68,10 +68,14 @@ def load():
         lib.wave_run_host.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
+        lib.stencil_plan_host_phases.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
+        lib.stencil_schedule_query.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_version.restype = ctypes.c_char_p
         for fn in ("stencil_apply", "stencil_apply_semi", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
                    "stencil_plan_status", "stencil_apply_host",
-                   "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject"):
+                   "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject",
+                   "stencil_schedule_query", "stencil_plan_host_phases"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -201,8 +205,27 @@ class StencilPlan:
         m = _check(self._lib.stencil_plan_launch_info(self._p, kind, buf, len(buf)))
         return {k: int(buf[i]) for i, k in enumerate(LAUNCH_INFO_KEYS[:m])}
 
+    def host_phases(self) -> dict:
+        """stencil_plan_host_phases: phase end times (ms) of the last pipelined host sweep."""
+        buf = (ctypes.c_float * 5)()
+        m = _check(self._lib.stencil_plan_host_phases(self._p, buf, 5))
+        keys = ("total_ms", "first_slab_in_ms", "copies_in_done_ms", "sweeps_done_ms", "slabs")
+        return {k: float(buf[i]) for i, k in enumerate(keys[:m])}
+
     def debug_inject(self, mode: int) -> None:
         _check(self._lib.stencil_debug_inject(self._p, int(mode)))
+
+
+SCHEDULE_KEYS = ("grid", "tiles", "zchunks", "items", "tile_x", "tile_y")
+
+
+def schedule_query(nx: int, ny: int, nz: int, radius: int, kind: int, num_sms: int,
+                   ctas_per_sm: int) -> dict:
+    """stencil_schedule_query: the plan's z-chunk schedule for a given GPU, host-only."""
+    buf = (ctypes.c_int64 * len(SCHEDULE_KEYS))()
+    m = _check(load().stencil_schedule_query(int(nx), int(ny), int(nz), int(radius), int(kind),
+                                             int(num_sms), int(ctas_per_sm), buf, len(buf)))
+    return {k: int(buf[i]) for i, k in enumerate(SCHEDULE_KEYS[:m])}
 
 
 def version() -> str:

@@ -84,6 +84,7 @@ struct stencil_plan {
   cudaStream_t pipe[3];  // copies in, compute, copies out
   cudaEvent_t ev[2 * 32 + 2];
   bool pipe_ready;
+  int pipe_slabs;        // slabs of the last pipelined call (0: none yet)
 };
 
 namespace {
@@ -95,10 +96,81 @@ bool interior_empty(const stencil_plan* p) {
   return p->nx < m || p->ny < m || p->nz < m;
 }
 
-// Launch geometry for the output planes [R + zoff, R + zoff + nzi) of the grid.  Choose
-// the number of z-chunks per tile column: minimise the per-CTA step count of the
-// round-robin schedule (a filling step costs about a third of a computing one); light
-// sweeps instead take the fewest chunks that occupy every SM.
+// The z-chunk schedule for `nzi` output planes of x-y tiles of height tile_y: the number
+// of chunks per tile column, minimising the per-CTA step count of the round-robin
+// schedule over `slots` CTA slots (a filling step costs about a third of a computing one);
+// light sweeps instead take the fewest chunks that occupy every SM.
+//
+// Only one chunk count per round count can win: with k rounds, n_k = floor(k * slots /
+// ntiles) chunks (at least 1, at most nzi) is the most that still fit, and any smaller n
+// with k rounds has as many rounds, no fewer steps per item and fewer busy slots.  The
+// scan therefore visits round counts, not chunk counts, and its cost does not grow with
+// nz (at most kMaxRounds candidates).
+struct Schedule {
+  int ntx, ntiles, nchunks, nitems, grid;
+};
+
+constexpr int64_t kMaxRounds = 1 << 14;
+
+Schedule schedule(int64_t nx, int64_t ny, int R, int tile_y, int kind, int num_sms, int occupancy,
+                  int nzi) {
+  Schedule sc{};
+  sc.ntx = (int)((nx + kTX - 1) / kTX);
+  const int nty = (int)((ny - 2 * R + tile_y - 1) / tile_y);
+  sc.ntiles = sc.ntx * nty;
+  const int64_t slots = (int64_t)num_sms * std::max(1, occupancy);
+  const int64_t ntiles = sc.ntiles;
+  // Cost of n chunks: rounds of the round-robin schedule x steps per item; and the share
+  // of the GPU's CTA slots the schedule keeps busy (a partly filled round idles the rest).
+  auto plan_n = [&](int64_t n, double& cost, double& busy) {
+    const int64_t items = ntiles * n;
+    const int64_t g = std::min<int64_t>(items, slots);
+    const int64_t rounds = (items + g - 1) / g;
+    cost = (double)rounds * ((double)((nzi + n - 1) / n) + 0.35 * 2 * R);
+    busy = (double)items / (double)(rounds * slots);
+  };
+  const int64_t max_n = std::min<int64_t>(nzi, ((int64_t)1 << 30) / ntiles);
+  auto candidate = [&](int64_t k) {
+    return std::min<int64_t>(max_n, std::max<int64_t>(1, k * slots / ntiles));
+  };
+  double best = 1e300, cost, busy;
+  for (int64_t k = 1, last = 0; k <= kMaxRounds; ++k) {
+    const int64_t n = candidate(k);
+    if (n == last) continue;
+    last = n;
+    plan_n(n, cost, busy);
+    best = std::min(best, cost);
+    if (n == max_n) break;
+  }
+  // Among near-ties (within 0.5 %), take the fullest schedule: at 1536 x 1536 x 256,
+  // R = 4, 1 and 5 chunks cost the same, and 5 (a 95 % full last round instead of 79 %)
+  // measured 5 % faster.
+  int64_t best_n = 1;
+  double best_busy = -1.0;
+  for (int64_t k = 1, last = 0; k <= kMaxRounds; ++k) {
+    const int64_t n = candidate(k);
+    if (n == last) continue;
+    last = n;
+    plan_n(n, cost, busy);
+    if (cost <= best * 1.005 && busy > best_busy + 1e-12) {
+      best_busy = busy;
+      best_n = n;
+    }
+    if (n == max_n) break;
+  }
+  if ((kind == 0 || kind == 3) && R <= 2) {
+    // Light sweeps are bound by memory traffic, not by the busiest SM: the fewest chunks
+    // that still give every SM a CTA keep the fewest z-fronts in flight and the fewest
+    // refilled planes (measured at 512^3, R = 1: 2 chunks 5.7 TB/s, 7 chunks 4.9 TB/s).
+    best_n = std::min<int64_t>(nzi, ((int64_t)num_sms + ntiles - 1) / ntiles);
+  }
+  sc.nchunks = (int)best_n;
+  sc.nitems = (int)(ntiles * best_n);
+  sc.grid = (int)std::min<int64_t>(sc.nitems, slots);
+  return sc;
+}
+
+// Launch geometry for the output planes [R + zoff, R + zoff + nzi) of the grid.
 void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp, int& grid) {
   const KernelDesc& kd = p->kd[kind];
   const int R = p->radius;
@@ -113,48 +185,14 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
     grid = 0;
     return;
   }
-  sp.ntx = (int)((p->nx + kTX - 1) / kTX);
-  const int nty = (int)((p->ny - 2 * R + kd.tile_y - 1) / kd.tile_y);
-  sp.ntiles = sp.ntx * nty;
+  const Schedule sc = schedule(p->nx, p->ny, R, kd.tile_y, kind, p->num_sms, p->occupancy[kind], nzi);
+  sp.ntx = sc.ntx;
+  sp.ntiles = sc.ntiles;
   sp.nzi = nzi;
   sp.zoff = zoff;
-  const int64_t slots = (int64_t)p->num_sms * std::max(1, p->occupancy[kind]);
-  // Cost of n chunks: rounds of the round-robin schedule x steps per item; and the share
-  // of the GPU's CTA slots the schedule keeps busy (a partly filled round idles the rest).
-  auto plan_n = [&](int n, double& cost, double& busy) {
-    const int64_t items = (int64_t)sp.ntiles * n;
-    const int64_t g = std::min<int64_t>(items, slots);
-    const int64_t rounds = (items + g - 1) / g;
-    cost = (double)rounds * ((double)((sp.nzi + n - 1) / n) + 0.35 * 2 * R);
-    busy = (double)items / (double)(rounds * slots);
-  };
-  const int max_n = (int)std::min<int64_t>(sp.nzi, ((int64_t)1 << 30) / sp.ntiles);
-  double best = 1e300, cost, busy;
-  for (int n = 1; n <= max_n; ++n) {
-    plan_n(n, cost, busy);
-    best = std::min(best, cost);
-  }
-  // Among near-ties (within 0.5 %), take the fullest schedule: at 1536 x 1536 x 256,
-  // R = 4, 1 and 5 chunks cost the same, and 5 (a 95 % full last round instead of 79 %)
-  // measured 5 % faster.
-  int best_n = 1;
-  double best_busy = -1.0;
-  for (int n = 1; n <= max_n; ++n) {
-    plan_n(n, cost, busy);
-    if (cost <= best * 1.005 && busy > best_busy + 1e-12) {
-      best_busy = busy;
-      best_n = n;
-    }
-  }
-  if ((kind == 0 || kind == 3) && R <= 2) {
-    // Light sweeps are bound by memory traffic, not by the busiest SM: the fewest chunks
-    // that still give every SM a CTA keep the fewest z-fronts in flight and the fewest
-    // refilled planes (measured at 512^3, R = 1: 2 chunks 5.7 TB/s, 7 chunks 4.9 TB/s).
-    best_n = (int)std::min<int64_t>(sp.nzi, ((int64_t)p->num_sms + sp.ntiles - 1) / sp.ntiles);
-  }
-  sp.nchunks = best_n;
-  sp.nitems = sp.ntiles * best_n;
-  grid = (int)std::min<int64_t>(sp.nitems, slots);
+  sp.nchunks = sc.nchunks;
+  sp.nitems = sc.nitems;
+  grid = sc.grid;
 }
 
 void plan_geometry(stencil_plan* p, int kind) {
@@ -329,8 +367,8 @@ int apply_host_pipelined(stencil_plan* p, const float* in_host, float* out_host,
   if (!p->pipe_ready) {
     for (cudaStream_t& q : p->pipe)
       if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking);
-    for (cudaEvent_t& v : p->ev)
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    for (cudaEvent_t& v : p->ev)  // timing events: stencil_plan_host_phases reads them
+      if (e == cudaSuccess) e = cudaEventCreate(&v);
     if (e != cudaSuccess) return cuda_fail(e, "pipeline streams");
     p->pipe_ready = true;
   }
@@ -364,6 +402,7 @@ int apply_host_pipelined(stencil_plan* p, const float* in_host, float* out_host,
   e = cudaEventRecord(done, hout);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(user, done, 0);
   if (e != cudaSuccess) return cuda_fail(e, "pipeline end");
+  p->pipe_slabs = K;
   return stencil_plan_status(p, user);
 }
 
@@ -646,6 +685,44 @@ int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int
   return m;
 }
 
+int stencil_plan_host_phases(const stencil_plan* p, float* ms, int n) {
+  if (!p || !ms || n < 0) return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (!p->pipe_ready || p->pipe_slabs < 1) return fail(STENCIL_ERR_ARG, "no pipelined host sweep has run");
+  const int K = p->pipe_slabs;
+  cudaEvent_t start = p->ev[2 * 32], done = p->ev[2 * 32 + 1];
+  float v[5] = {0, 0, 0, 0, (float)K};
+  cudaError_t e = cudaEventElapsedTime(&v[0], start, done);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&v[1], start, p->ev[0]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&v[2], start, p->ev[K - 1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&v[3], start, p->ev[32 + K - 1]);
+  if (e != cudaSuccess) return cuda_fail(e, "host phase events");
+  const int m = std::min(n, 5);
+  for (int i = 0; i < m; ++i) ms[i] = v[i];
+  return m;
+}
+
+int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int kind, int num_sms,
+                           int ctas_per_sm, int64_t* info, int n) {
+  if (radius < 1 || radius > STENCIL_MAX_RADIUS || kind < 0 || kind > 3 || num_sms < 1 ||
+      ctas_per_sm < 1 || !info || n < 0)
+    return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (nx < 1 || ny < 1 || nz < 1 || nx > (1 << 30) || ny > (1 << 30) || nz > (1 << 30) ||
+      nx * ny > ((int64_t)1 << 40) || nx * ny * nz > ((int64_t)1 << 40))
+    return fail(STENCIL_ERR_ARG, "grid %lld x %lld x %lld out of range", (long long)nx,
+                (long long)ny, (long long)nz);
+  const KernelDesc kd = kind == 0   ? apply_kernel_desc(radius)
+                        : kind == 3 ? semi_kernel_desc(radius)
+                                    : wave_kernel_desc(radius, kind == 2);
+  const int64_t m = 2 * (int64_t)radius + 1;
+  Schedule sc{};
+  if (nx >= m && ny >= m && nz >= m)
+    sc = schedule(nx, ny, radius, kd.tile_y, kind, num_sms, ctas_per_sm, (int)(nz - 2 * radius));
+  const int64_t v[6] = {sc.grid, sc.ntiles, sc.nchunks, sc.nitems, kTX, kd.tile_y};
+  const int k = std::min(n, 6);
+  for (int i = 0; i < k; ++i) info[i] = v[i];
+  return k;
+}
+
 int stencil_debug_inject(stencil_plan* p, int mode) {
   if (!p || mode < 0 || mode > 1) return fail(STENCIL_ERR_ARG, "bad arguments");
   p->debug_mode = mode;
@@ -657,37 +734,27 @@ int stencil_debug_inject(stencil_plan* p, int mode) {
 // ---- allocation-free sweep ---------------------------------------------------------
 //
 // Some callers cannot allocate device memory at the time they need a sweep: code that
-// runs inside another framework's memory pool which owns all free device memory, a
-// process with a fixed device-memory budget decided at start-up, or a host callback
-// where an allocation could deadlock with the caller's allocator.  For them,
+// runs inside another framework's memory pool which owns all free device memory, or a
+// process whose device-memory footprint is fixed at start-up.  For them,
 // stencil_apply_noalloc runs the same sweep kernel as stencil_apply, with the kernel's
 // status block placed in the file-scope device array below instead of plan-owned
 // memory, and builds its plan on the stack.
 //
 // In host code `g_noalloc_scratch` names a host-side stand-in, not the device copy:
 // passing it to a kernel would fault (or, where the GPU can reach host memory, silently
-// use the wrong memory).  Its device address is obtained with cudaGetSymbolAddress
-// once per device, with that device current, and cached.
+// use the wrong memory).  Every call asks cudaGetSymbolAddress for the array's address
+// in the current device's context (a lookup, no allocation); nothing is cached, so a
+// context that was reset and re-created since the previous call gets its own address.
 namespace {
 
 constexpr int kNoAllocScratchWords = 64;  // 256 bytes; the sweep uses the first 4 words
 __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocScratchWords];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-unsigned* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
-
-int noalloc_scratch(int device, unsigned** out) {
-  if (device < 0 || device >= kMaxDevices)
-    return fail(STENCIL_ERR_ARG, "device ordinal %d beyond %d", device, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[device]) {
-    void* ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    g_noalloc_ptr[device] = static_cast<unsigned*>(ptr);
-  }
-  *out = g_noalloc_ptr[device];
+int noalloc_scratch(unsigned** out) {
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+  *out = static_cast<unsigned*>(ptr);
   return STENCIL_OK;
 }
 
@@ -718,7 +785,7 @@ extern "C" int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int rad
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, pl.device);
   if (e != cudaSuccess) return cuda_fail(e, "device query");
-  int rc = noalloc_scratch(pl.device, &pl.d_status);
+  int rc = noalloc_scratch(&pl.d_status);
   if (rc) return rc;
   pl.kd[0] = apply_kernel_desc(radius);
   e = cudaFuncSetAttribute(pl.kd[0].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.kd[0].smem);

@@ -97,13 +97,23 @@ def test_host_buffer_entry_matches_device_path():
     plan.close()
 
 
-def test_wave25_640_hundred_steps():
+@pytest.fixture(scope="module")
+def wave640():
+    """The 640^3 acoustic workload's inputs and the oracle's independent 100-step run."""
+    n = 640
+    up, u, s, e = synth.wave_fields(n, n, n)
+    c = synth.laplacian8_coeffs()
+    o_prev, o_cur = oracle.run_wave(up, u, s, e, c.astype(np.float32), 4, 100)
+    return {"fields": (up, u, s, e), "c": c, "o_prev": o_prev, "o_cur": o_cur}
+
+
+def test_wave25_640_hundred_steps(wave640):
     """The 640^3 acoustic run: 100 steps on the GPU and in the oracle from identical
     inputs, relative L2 <= 1e-4; plus a per-step sampled check on the GPU's own state."""
     torch = torch_cuda()
     n = 640
-    up, u, s, e = synth.wave_fields(n, n, n)
-    c = synth.laplacian8_coeffs()
+    up, u, s, e = wave640["fields"]
+    c = wave640["c"]
     c32 = c.astype(np.float32)
     plan = StencilPlan(n, n, n, 4, c)
     d = [torch.from_numpy(a.ravel()).cuda() for a in (up, u, s, e)]
@@ -123,10 +133,32 @@ def test_wave25_640_hundred_steps():
     plan.status(None, b)
     g_cur = b.cpu().numpy().reshape(u.shape)
     plan.close()
-    o_prev, o_cur = oracle.run_wave(up, u, s, e, c32, 4, 100)
-    r = rel_l2(g_cur, o_cur)
-    print(f"wave25 640^3 x100: relative L2 {r:.3e}, |u|_2 {np.linalg.norm(o_cur):.4f}")
+    r = rel_l2(g_cur, wave640["o_cur"])
+    print(f"wave25 640^3 x100: relative L2 {r:.3e}, |u|_2 {np.linalg.norm(wave640['o_cur']):.4f}")
     assert r <= 1e-4
+
+
+@pytest.mark.parametrize("pml", [-1, 16])
+def test_native_wave_steps_640_match_oracle(wave640, pml):
+    """The 640^3 workload as the benchmark runs it: wave_steps, all 100 steps captured once
+    as a CUDA graph (pml < 0: wave_step; 16: wave_step_pml with the 16-point sponge band),
+    against the oracle's run: relative L2 <= 1e-4 for the last two levels."""
+    torch = torch_cuda()
+    n = 640
+    up, u, s, e = wave640["fields"]
+    c = wave640["c"]
+    plan = StencilPlan(n, n, n, 4, c)
+    f = [torch.from_numpy(x.ravel()).cuda() for x in (up, u, s, e)]
+    bufs = [f[0], f[1], f[0].clone()]
+    plan.wave_steps(bufs[0], bufs[1], bufs[2], f[2], f[3], 100, pml_width=pml, use_graph=True)
+    plan.status(None, bufs[0])
+    cur = bufs[101 % 3].cpu().numpy().reshape(u.shape)
+    prev = bufs[100 % 3].cpu().numpy().reshape(u.shape)
+    plan.close()
+    del f, bufs
+    r_cur, r_prev = rel_l2(cur, wave640["o_cur"]), rel_l2(prev, wave640["o_prev"])
+    print(f"wave_steps 640^3 x100 (pml {pml}): relative L2 {r_cur:.3e} / {r_prev:.3e}")
+    assert r_cur <= 1e-4 and r_prev <= 1e-4
 
 
 def band_mask(shape, width):

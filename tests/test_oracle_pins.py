@@ -326,6 +326,73 @@ def test_exact_discrete_leapfrog(oracle_mod, eta):
     assert abs(g(40)) > 1e-3 or eta > 0
 
 
+def _leapfrog_gain(lam, s, eta):
+    """g(n) of the per-mode recurrence (1+eta) g[n+1] = (2 + s lam) g[n] - (1-eta) g[n-1],
+    g[-1] = g[0] = 1, evaluated by the recurrence itself in exact rational-free floats."""
+    g = {-1: 1.0, 0: 1.0}
+
+    def at(n):
+        for k in range(max(g) + 1, n + 1):
+            g[k] = ((2.0 + s * lam) * g[k - 1] - (1.0 - eta) * g[k - 2]) / (1.0 + eta)
+        return g[n]
+    return at
+
+
+def _face_distance(shape):
+    nz, ny, nx = shape
+    return np.minimum.reduce(np.meshgrid(np.minimum(np.arange(nz), nz - 1 - np.arange(nz)),
+                                         np.minimum(np.arange(ny), ny - 1 - np.arange(ny)),
+                                         np.minimum(np.arange(nx), nx - 1 - np.arange(nx)), indexing="ij"))
+
+
+@pytest.mark.parametrize("R,coeffs,nsteps,shape", [(4, "lap8", 6, (60, 58, 62)),
+                                                    (1, "lap2", 17, (48, 46, 44))])
+@pytest.mark.parametrize("eta", [0.0, 0.05])
+def test_run_wave_time_loop_on_an_eigenmode(oracle_mod, R, coeffs, nsteps, shape, eta):
+    """The oracle's own time loop (three-buffer rotation, fixed shell) on an eigenmode.
+
+    run_wave keeps every buffer's shell at its starting value u0, so its levels differ
+    from the exact g(n) u0 only where the fixed shell has reached: level n is exact at
+    every point at least n*R from the nearest face (level 1 reads only level 0 and its
+    shell, which are exact; each later level moves the front R points inward). On that
+    core both returned levels must equal g(n-1) u0 and g(n) u0, the per-mode leapfrog
+    recurrence; a slip in the rotation (levels swapped, a level reused) breaks it at once.
+    Outside the core the fixed shell must have made a difference, or the pin would not
+    see the rotation of the shell values either.
+    """
+    c = LAP8 if coeffs == "lap8" else LAP2
+    th, s = (0.7, 1.3, 2.1), 0.2
+    lam = sum(c[0] / 3.0 + 2.0 * sum(c[r] * math.cos(r * t) for r in range(1, R + 1)) for t in th)
+    g = _leapfrog_gain(lam, s, eta)
+    u0 = _eigenmode(shape, th)
+    S = np.full(shape, s)
+    E = np.full(shape, eta)
+    prev, cur = oracle_mod.run_wave(u0, u0, S, E, c, R, nsteps)
+    core = _face_distance(shape) >= nsteps * R
+    assert core.sum() > 1000
+    np.testing.assert_allclose(cur[core], g(nsteps) * u0[core], rtol=0, atol=1e-10)
+    np.testing.assert_allclose(prev[core], g(nsteps - 1) * u0[core], rtol=0, atol=1e-10)
+    ring = (_face_distance(shape) >= R) & ~core
+    assert np.max(np.abs(cur[ring] - g(nsteps) * u0[ring])) > 1e-6
+    # the inputs are not modified
+    np.testing.assert_array_equal(u0, _eigenmode(shape, th))
+
+
+def test_run_wave_zero_and_one_step(oracle_mod):
+    """Zero steps return the inputs; one step equals one wave_step."""
+    shape = (14, 13, 12)
+    up = rng(31).uniform(-1, 1, shape)
+    u = rng(32).uniform(-1, 1, shape)
+    s = rng(33).uniform(0, 0.2, shape)
+    e = rng(34).uniform(0, 0.1, shape)
+    a, b = oracle_mod.run_wave(up, u, s, e, LAP8, 4, 0)
+    np.testing.assert_array_equal(a, up)
+    np.testing.assert_array_equal(b, u)
+    a, b = oracle_mod.run_wave(up, u, s, e, LAP8, 4, 1)
+    np.testing.assert_array_equal(a, u)
+    np.testing.assert_array_equal(b, oracle_mod.wave_step(up, u, s, e, LAP8, 4))
+
+
 def test_sweeps_keep_a_fixed_shell(oracle_mod):
     u0 = rng(19).uniform(-1, 1, (10, 11, 12)).astype(np.float32)
     out = oracle_mod.run_sweeps(u0, LAP2.astype(np.float32), 1, 3)

@@ -3,13 +3,15 @@
 Some callers cannot allocate device memory at the moment they need a sweep (their
 framework's pool owns the free memory, or their footprint is fixed at start-up); this
 entry point serves them by keeping its scratch in a fixed device array inside the
-library.  Its output must match the plan-based stencil_apply on the same input, on two
-calls in a row (the second call reuses the scratch the first one left behind).
+library.  Its output must match the CPU oracle and the plan-based stencil_apply on the
+same input, on two calls in a row (the second call reuses the scratch the first one left
+behind), and a call must not take any device memory.
 This file is collected last so that a failure here never hides the other tests.
 """
 import numpy as np
 import pytest
 
+import oracle
 from seismic_wave_propagation_gb300 import StencilError, StencilPlan, synth
 from seismic_wave_propagation_gb300._lib import apply_noalloc
 from gpu_util import interior_mask, sweep_tol, torch_cuda
@@ -21,9 +23,10 @@ pytestmark = pytest.mark.gpu
     (136, 75, 41, 4, "laplacian8"),
     (64, 64, 64, 1, "average7"),
 ])
-def test_noalloc_matches_plan_apply_twice(nx, ny, nz, R, coeffs):
+def test_noalloc_matches_oracle_and_plan_apply_twice(nx, ny, nz, R, coeffs):
     torch = torch_cuda()
     c = synth.coeffs_for(coeffs)
+    c32 = c.astype(np.float32)
     plan = StencilPlan(nx, ny, nz, R, c)
     m = interior_mask((nz, ny, nx), R)
     for call, seed in enumerate((11, 12)):
@@ -36,10 +39,35 @@ def test_noalloc_matches_plan_apply_twice(nx, ny, nz, R, coeffs):
         apply_noalloc(nx, ny, nz, R, c, d_in, got)
         ref_h = ref.cpu().numpy().reshape(u.shape)
         got_h = got.cpu().numpy().reshape(u.shape)
-        tol = sweep_tol(c, u)
-        assert np.max(np.abs(got_h[m].astype(np.float64) - ref_h[m])) <= tol, f"call {call}"
+        want = oracle.apply(u, c32, R)
+        tol = sweep_tol(c32, u)
+        assert np.max(np.abs(got_h[m].astype(np.float64) - want[m])) <= tol, f"call {call} vs oracle"
+        assert np.max(np.abs(got_h[m].astype(np.float64) - ref_h[m])) <= tol, f"call {call} vs stencil_apply"
         np.testing.assert_array_equal(got_h[~m], u[~m])  # shell untouched
     plan.close()
+
+
+def test_noalloc_takes_no_device_memory():
+    """After a first call (which may load the library's device code), a call on a grid of
+    another shape leaves the device's free memory unchanged."""
+    torch = torch_cuda()
+    c = synth.laplacian8_coeffs()
+    a = torch.from_numpy(synth.uniform_field(72, 40, 30, seed=5).ravel()).cuda()
+    b = a.clone()
+    apply_noalloc(72, 40, 30, 4, c, a, b)
+    u = synth.uniform_field(200, 66, 52, seed=6)
+    d_in = torch.from_numpy(u.ravel()).cuda()
+    d_out = d_in.clone()
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    apply_noalloc(200, 66, 52, 4, c, d_in, d_out)
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after >= free_before, f"free device memory fell by {free_before - free_after} bytes"
+    got = d_out.cpu().numpy().reshape(u.shape)
+    want = oracle.apply(u, c.astype(np.float32), 4)
+    m = interior_mask(u.shape, 4)
+    assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= sweep_tol(c.astype(np.float32), u)
 
 
 def test_noalloc_rejects_bad_sizes():
