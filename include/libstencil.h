@@ -233,6 +233,46 @@ int stencil_debug_inject(stencil_plan* plan, int mode);
 int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int radius, const float* coeffs,
                           const float* in, float* out, void* stream);
 
+/*
+ * z-slab decomposition.  The grid is cut along z into `nslabs` slabs; slab k owns the
+ * global planes [o_k, o_k+1), o_k = floor(k * nz / nslabs), and is stored as a separate
+ * nx x ny x (e_k - s_k) device array holding the global planes [s_k, e_k) =
+ * [max(0, o_k - R), min(nz, o_k+1 + R)): its owned planes plus up to R ghost planes on
+ * each side (plane z of the grid is plane z - s_k of the slab array, x innermost as
+ * everywhere).  Every slab must own at least R planes.  Each slab array has the layout,
+ * alignment and shell rules of a field of stencil_apply; the ghost planes are slab-local
+ * shell, which no sweep writes.
+ *
+ * The path shards this way along z, one ghost exchange of R planes each way per cut and
+ * per sweep or step.  Here every slab lives on the device current at creation; the calls
+ * copy ghost planes between slab arrays with device-to-device copies on an internal
+ * stream, overlapped with the output planes that read no ghost plane.
+ *
+ * stencil_slabs_create:   plans for every slab (coeffs and radius as stencil_plan_create);
+ *                         NULL on failure (stencil_last_error says why).
+ * stencil_slabs_extent:   info[0..n) = s_k, e_k, o_k, o_k+1 (global planes) of slab k.
+ * stencil_slabs_exchange: fill every ghost plane of the field's slabs from its owner.
+ * stencil_slabs_apply:    one sweep of the whole grid: exchange ghost planes of `in`, then
+ *                         stencil_apply on every slab; out[k] gets slab k's owned interior
+ *                         planes (its shell and ghost planes are untouched).
+ * stencil_slabs_wave_step: one wave step of the whole grid (ghosts of `u` exchanged; the
+ *                         other fields are read only at the output points).  u_next[k] ==
+ *                         u_prev[k] for every slab is allowed (two-buffer stepping).
+ * stencil_slabs_status:   stencil_plan_status of every slab's plan.
+ * Fields are host arrays of nslabs device pointers; no two slab arrays may overlap
+ * (STENCIL_ERR_ALIAS).  Errors as for stencil_apply / wave_step.
+ */
+typedef struct stencil_slabs stencil_slabs; /* opaque */
+stencil_slabs* stencil_slabs_create(int64_t nx, int64_t ny, int64_t nz, int radius, const float* coeffs,
+                                    int nslabs);
+void stencil_slabs_destroy(stencil_slabs* slabs);
+int stencil_slabs_extent(const stencil_slabs* slabs, int k, int64_t* info, int n);
+int stencil_slabs_exchange(stencil_slabs* slabs, float* const* fields, void* stream);
+int stencil_slabs_apply(stencil_slabs* slabs, float* const* in, float* const* out, void* stream);
+int stencil_slabs_wave_step(stencil_slabs* slabs, float* const* u_prev, float* const* u,
+                            float* const* u_next, float* const* v2dt2, float* const* eta, void* stream);
+int stencil_slabs_status(stencil_slabs* slabs, void* stream);
+
 /* Library version string. */
 const char* stencil_version(void);
 

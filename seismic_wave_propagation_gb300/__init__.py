@@ -7,8 +7,8 @@ Importing the package does not load the library; the first plan does, and raises
 has not been built.
 """
 from ._lib import (KIND_APPLY, KIND_SEMI, KIND_WAVE, KIND_WAVE_PML, StencilError, StencilPlan,  # noqa: F401
-                   last_error, load, version)
+                   StencilSlabs, last_error, load, version)
 from . import synth, traffic  # noqa: F401
 
-__all__ = ["StencilPlan", "StencilError", "KIND_APPLY", "KIND_WAVE", "KIND_WAVE_PML", "KIND_SEMI", "load", "last_error",
+__all__ = ["StencilPlan", "StencilSlabs", "StencilError", "KIND_APPLY", "KIND_WAVE", "KIND_WAVE_PML", "KIND_SEMI", "load", "last_error",
            "version", "synth", "traffic"]

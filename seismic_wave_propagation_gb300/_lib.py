@@ -72,10 +72,21 @@ def load():
         lib.stencil_schedule_query.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_version.restype = ctypes.c_char_p
+        lib.stencil_slabs_create.argtypes = [i64, i64, i64, ctypes.c_int, fp, ctypes.c_int]
+        lib.stencil_slabs_create.restype = vp
+        lib.stencil_slabs_destroy.argtypes = [vp]
+        lib.stencil_slabs_destroy.restype = None
+        lib.stencil_slabs_extent.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
+        lib.stencil_slabs_exchange.argtypes = [vp, vp, vp]
+        lib.stencil_slabs_apply.argtypes = [vp, vp, vp, vp]
+        lib.stencil_slabs_wave_step.argtypes = [vp] * 7
+        lib.stencil_slabs_status.argtypes = [vp, vp]
         for fn in ("stencil_apply", "stencil_apply_semi", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
                    "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject",
-                   "stencil_schedule_query", "stencil_plan_host_phases"):
+                   "stencil_schedule_query", "stencil_plan_host_phases", "stencil_slabs_extent",
+                   "stencil_slabs_exchange", "stencil_slabs_apply", "stencil_slabs_wave_step",
+                   "stencil_slabs_status"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -214,6 +225,63 @@ class StencilPlan:
 
     def debug_inject(self, mode: int) -> None:
         _check(self._lib.stencil_debug_inject(self._p, int(mode)))
+
+
+class StencilSlabs:
+    """The grid cut along z into slabs, each its own device array with ghost planes
+    (stencil_slabs_* in include/libstencil.h).  Fields are lists of per-slab arrays."""
+
+    def __init__(self, nx: int, ny: int, nz: int, radius: int, coeffs, nslabs: int):
+        lib = load()
+        c = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32))
+        self.nx, self.ny, self.nz, self.radius, self.nslabs = int(nx), int(ny), int(nz), int(radius), int(nslabs)
+        self._p = lib.stencil_slabs_create(self.nx, self.ny, self.nz, self.radius,
+                                           c.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), self.nslabs)
+        if not self._p:
+            raise StencilError(-1, last_error())
+        self._lib = lib
+
+    def extent(self, k: int) -> dict:
+        """Global planes of slab k: stored [begin, end) (ghosts included), owned [own_begin, own_end)."""
+        buf = (ctypes.c_int64 * 4)()
+        _check(self._lib.stencil_slabs_extent(self._p, int(k), buf, 4))
+        return {"begin": buf[0], "end": buf[1], "own_begin": buf[2], "own_end": buf[3]}
+
+    def slab_shape(self, k: int) -> tuple:
+        e = self.extent(k)
+        return (e["end"] - e["begin"], self.ny, self.nx)
+
+    def _ptrs(self, fields):
+        if len(fields) != self.nslabs:
+            raise ValueError(f"need {self.nslabs} slab arrays")
+        arr = (ctypes.c_void_p * self.nslabs)(*[_addr(f) for f in fields])
+        return arr
+
+    def exchange(self, fields, stream=None) -> None:
+        _check(self._lib.stencil_slabs_exchange(self._p, self._ptrs(fields), _stream(stream, *fields)))
+
+    def apply(self, inp, out, stream=None) -> None:
+        _check(self._lib.stencil_slabs_apply(self._p, self._ptrs(inp), self._ptrs(out),
+                                             _stream(stream, *inp, *out)))
+
+    def wave_step(self, u_prev, u, u_next, v2dt2, eta, stream=None) -> None:
+        f = (u_prev, u, u_next, v2dt2, eta)
+        _check(self._lib.stencil_slabs_wave_step(self._p, *[self._ptrs(x) for x in f],
+                                                 _stream(stream, *u)))
+
+    def status(self, stream=None, *fields) -> None:
+        _check(self._lib.stencil_slabs_status(self._p, _stream(stream, *fields)))
+
+    def close(self):
+        if getattr(self, "_p", None):
+            self._lib.stencil_slabs_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 SCHEDULE_KEYS = ("grid", "tiles", "zchunks", "items", "tile_x", "tile_y")

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "libstencil.h"
 #include "kernel_table.h"
@@ -814,3 +815,240 @@ extern "C" int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int rad
                 h[0], h[1], h[2]);
   return STENCIL_OK;
 }
+
+// ---- z-slab decomposition ----------------------------------------------------------
+//
+// The grid is cut along z into slabs; slab k owns the global planes [o_k, o_k+1) and
+// stores them with up to R ghost planes on each side, [s_k, e_k) = [max(0, o_k - R),
+// min(nz, o_k+1 + R)), as an nx x ny x (e_k - s_k) array of its own.  Its local interior
+// is then exactly its owned interior planes, so a sweep of the whole grid is one sweep
+// per slab once every ghost plane holds its owner's current values.  The exchange is one
+// copy of R planes each way per cut; the output planes that read no ghost plane run
+// while the copies are in flight, the 2R planes next to each cut after them.
+struct stencil_slabs {
+  int64_t nx, ny, nz;
+  int radius;
+  int nslabs;
+  int device;
+  std::vector<int64_t> own;           // o_0 .. o_P
+  std::vector<stencil_plan*> plans;   // one per slab, for its stored planes
+  cudaStream_t copy;                  // the exchange's stream
+  cudaEvent_t fork, join;
+};
+
+namespace {
+
+int64_t slab_begin(const stencil_slabs* S, int k) { return std::max<int64_t>(0, S->own[k] - S->radius); }
+int64_t slab_end(const stencil_slabs* S, int k) { return std::min<int64_t>(S->nz, S->own[k + 1] + S->radius); }
+
+int check_slab_fields(stencil_slabs* S, float* const* f, const char* name) {
+  if (!f) return fail(STENCIL_ERR_ARG, "%s is NULL", name);
+  for (int k = 0; k < S->nslabs; ++k) {
+    char what[64];
+    snprintf(what, sizeof what, "%s[%d]", name, k);
+    const int rc = check_field(S->plans[k], f[k], what);
+    if (rc) return rc;
+  }
+  return STENCIL_OK;
+}
+
+size_t slab_bytes(const stencil_slabs* S, int k) {
+  return (size_t)(S->nx * S->ny * (slab_end(S, k) - slab_begin(S, k))) * 4;
+}
+
+// No two of the listed slab arrays may overlap (one field's slabs, or two fields).
+int check_slab_overlaps(const stencil_slabs* S, float* const* const* fields, int nfields) {
+  for (int f = 0; f < nfields; ++f)
+    for (int g = f; g < nfields; ++g)
+      for (int j = 0; j < S->nslabs; ++j)
+        for (int k = (f == g ? j + 1 : 0); k < S->nslabs; ++k) {
+          const float* a = fields[f][j];
+          const float* b = fields[g][k];
+          const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+          if (x < y + slab_bytes(S, k) && y < x + slab_bytes(S, j))
+            return fail(STENCIL_ERR_ALIAS, "slab arrays overlap (field %d slab %d, field %d slab %d)", f,
+                        j, g, k);
+        }
+  return STENCIL_OK;
+}
+
+// Ghost copies of every cut on stream s: slab c-1's top ghosts from slab c's first owned
+// planes, slab c's bottom ghosts from slab c-1's last owned planes.
+int slab_exchange(stencil_slabs* S, float* const* f, cudaStream_t s) {
+  const int R = S->radius;
+  const size_t plane = (size_t)S->nx * S->ny;
+  for (int c = 1; c < S->nslabs; ++c) {
+    const int64_t cut = S->own[c];
+    const int64_t lo = slab_begin(S, c - 1), hi = slab_begin(S, c);
+    cudaError_t e = cudaMemcpyAsync(f[c - 1] + (size_t)(cut - lo) * plane, f[c] + (size_t)(cut - hi) * plane,
+                                    (size_t)R * plane * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(f[c] + (size_t)(cut - R - hi) * plane, f[c - 1] + (size_t)(cut - R - lo) * plane,
+                          (size_t)R * plane * 4, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ghost exchange");
+  }
+  return STENCIL_OK;
+}
+
+// One sweep (kind 0) or wave step (kind 1) of every slab: the exchange of `x` (the field
+// the stencil reads) on the exchange stream, overlapped with the output planes that read
+// no ghost plane; then the planes next to the cuts.
+int slab_run(stencil_slabs* S, int kind, float* const* x, float* const* uprev, float* const* v2dt2,
+             float* const* eta, float* const* out, cudaStream_t s) {
+  const int R = S->radius;
+  const int P = S->nslabs;
+  // Local output-plane ranges per slab: [a, b) first, then the dependent ranges.
+  std::vector<int64_t> in_lo(P), in_hi(P);
+  for (int k = 0; k < P; ++k) {
+    const int64_t nzk = slab_end(S, k) - slab_begin(S, k);
+    in_lo[k] = k > 0 ? 2 * R : R;
+    in_hi[k] = k < P - 1 ? nzk - 2 * R : nzk - R;
+    if (in_hi[k] - in_lo[k] < R) in_lo[k] = in_hi[k] = R;  // too thin to split: all after the copies
+  }
+  auto run = [&](int k, int64_t lo, int64_t hi, cudaStream_t st) {
+    if (hi <= lo) return (int)STENCIL_OK;
+    stencil_plan* p = S->plans[k];
+    return launch(p, kind, x[k], uprev ? uprev[k] : nullptr, v2dt2 ? v2dt2[k] : nullptr,
+                  eta ? eta[k] : nullptr, out[k], st, 1 << 30, (int)(lo - R), (int)(hi - lo));
+  };
+  if (P > 1) {
+    cudaError_t e = cudaEventRecord(S->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(S->copy, S->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "exchange fork");
+  }
+  for (int k = 0; k < P; ++k) {
+    const int rc = run(k, in_lo[k], in_hi[k], s);
+    if (rc) return rc;
+  }
+  if (P > 1) {
+    int rc = slab_exchange(S, x, S->copy);
+    if (rc) return rc;
+    cudaError_t e = cudaEventRecord(S->join, S->copy);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, S->join, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "exchange join");
+  }
+  for (int k = 0; k < P; ++k) {
+    const int64_t nzk = slab_end(S, k) - slab_begin(S, k);
+    int rc;
+    if (in_hi[k] <= in_lo[k]) {
+      rc = run(k, R, nzk - R, s);
+    } else {
+      rc = run(k, R, in_lo[k], s);
+      if (!rc) rc = run(k, in_hi[k], nzk - R, s);
+    }
+    if (rc) return rc;
+  }
+  return STENCIL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+stencil_slabs* stencil_slabs_create(int64_t nx, int64_t ny, int64_t nz, int radius, const float* coeffs,
+                                    int nslabs) {
+  g_err[0] = 0;
+  if (nslabs < 1) {
+    fail(STENCIL_ERR_ARG, "nslabs %d < 1", nslabs);
+    return nullptr;
+  }
+  if (radius >= 1 && nz / nslabs < radius) {
+    fail(STENCIL_ERR_ARG, "%d slabs of %lld planes: every slab must own at least radius = %d planes",
+         nslabs, (long long)nz, radius);
+    return nullptr;
+  }
+  stencil_slabs* S = new stencil_slabs();
+  S->nx = nx;
+  S->ny = ny;
+  S->nz = nz;
+  S->radius = radius;
+  S->nslabs = nslabs;
+  for (int k = 0; k <= nslabs; ++k) S->own.push_back(nz * k / nslabs);
+  for (int k = 0; k < nslabs; ++k) {
+    stencil_plan* p = stencil_plan_create(nx, ny, slab_end(S, k) - slab_begin(S, k), radius, coeffs);
+    if (!p) {
+      stencil_slabs_destroy(S);
+      return nullptr;
+    }
+    S->plans.push_back(p);
+  }
+  S->device = S->plans[0]->device;
+  cudaError_t e = cudaStreamCreateWithFlags(&S->copy, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&S->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&S->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "slab streams");
+    stencil_slabs_destroy(S);
+    return nullptr;
+  }
+  return S;
+}
+
+void stencil_slabs_destroy(stencil_slabs* S) {
+  if (!S) return;
+  for (stencil_plan* p : S->plans) stencil_plan_destroy(p);
+  if (S->copy) cudaStreamDestroy(S->copy);
+  if (S->fork) cudaEventDestroy(S->fork);
+  if (S->join) cudaEventDestroy(S->join);
+  delete S;
+}
+
+int stencil_slabs_extent(const stencil_slabs* S, int k, int64_t* info, int n) {
+  if (!S || !info || n < 0 || k < 0 || k >= S->nslabs) return fail(STENCIL_ERR_ARG, "bad arguments");
+  const int64_t v[4] = {slab_begin(S, k), slab_end(S, k), S->own[k], S->own[k + 1]};
+  const int m = std::min(n, 4);
+  for (int i = 0; i < m; ++i) info[i] = v[i];
+  return m;
+}
+
+int stencil_slabs_exchange(stencil_slabs* S, float* const* fields, void* stream) {
+  if (!S) return fail(STENCIL_ERR_ARG, "slabs is NULL");
+  int rc = check_device(S->plans[0]);
+  if (rc || (rc = check_slab_fields(S, fields, "fields"))) return rc;
+  float* const* all[1] = {fields};
+  if ((rc = check_slab_overlaps(S, all, 1))) return rc;
+  return slab_exchange(S, fields, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_slabs_apply(stencil_slabs* S, float* const* in, float* const* out, void* stream) {
+  if (!S) return fail(STENCIL_ERR_ARG, "slabs is NULL");
+  int rc = check_device(S->plans[0]);
+  if (rc || (rc = check_slab_fields(S, in, "in")) || (rc = check_slab_fields(S, out, "out"))) return rc;
+  float* const* all[2] = {in, out};
+  if ((rc = check_slab_overlaps(S, all, 2))) return rc;
+  return slab_run(S, 0, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_slabs_wave_step(stencil_slabs* S, float* const* u_prev, float* const* u, float* const* u_next,
+                            float* const* v2dt2, float* const* eta, void* stream) {
+  if (!S) return fail(STENCIL_ERR_ARG, "slabs is NULL");
+  int rc = check_device(S->plans[0]);
+  if (rc || (rc = check_slab_fields(S, u_prev, "u_prev")) || (rc = check_slab_fields(S, u, "u")) ||
+      (rc = check_slab_fields(S, u_next, "u_next")) || (rc = check_slab_fields(S, v2dt2, "v2dt2")) ||
+      (rc = check_slab_fields(S, eta, "eta")))
+    return rc;
+  // u_next == u_prev (every slab) is allowed, as for wave_step.
+  const bool two_buffers = u_next[0] == u_prev[0];
+  for (int k = 0; k < S->nslabs; ++k)
+    if ((u_next[k] == u_prev[k]) != two_buffers)
+      return fail(STENCIL_ERR_ALIAS, "u_next equals u_prev for some slabs only");
+  if (two_buffers) {
+    float* const* all[4] = {u, u_next, v2dt2, eta};
+    if ((rc = check_slab_overlaps(S, all, 4))) return rc;
+  } else {
+    float* const* all[5] = {u_prev, u, u_next, v2dt2, eta};
+    if ((rc = check_slab_overlaps(S, all, 5))) return rc;
+  }
+  return slab_run(S, 1, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_slabs_status(stencil_slabs* S, void* stream) {
+  if (!S) return fail(STENCIL_ERR_ARG, "slabs is NULL");
+  for (stencil_plan* p : S->plans) {
+    const int rc = stencil_plan_status(p, stream);
+    if (rc) return rc;
+  }
+  return STENCIL_OK;
+}
+
+}  // extern "C"
