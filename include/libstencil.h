@@ -119,6 +119,23 @@ int wave_step_pml(stencil_plan* plan, const float* u_prev, const float* u, float
                   const float* v2dt2, const float* eta, int64_t pml_width, void* stream);
 
 /*
+ * Damping field of a PML whose computation reads eta through a 7-point stencil
+ * ("Accelerating High-Order Stencils on GPUs": in the PML region the computations on eta
+ * use a low-order 7-point stencil, halo one; the page prints no formula).  Reading: the
+ * damping at a point is the radius-1 star stencil of eta,
+ *   eta_eff = e0*eta + e1*(eta at the six face neighbours),
+ * at every point at least one away from every face (the faces of eta_eff get eta's
+ * values).  eta does not change in time, so this runs once per model: every later
+ * wave_step / wave_step_pml / wave_steps with eta_eff in place of eta is the step with the
+ * 7-point damping, at the cost of the pointwise step.  With e0 + 6*e1 = 1 a constant eta
+ * is left unchanged.  eta, eta_eff: device, nx*ny*nz floats, 16-byte aligned, must not
+ * overlap.  The first call creates a radius-1 plan of the grid inside the plan.
+ * Errors: STENCIL_ERR_ARG, _ALIGNMENT, _ALIAS, _CUDA.
+ */
+int wave_eta_stencil(stencil_plan* plan, const float* eta, float* eta_eff, float e0, float e1,
+                     void* stream);
+
+/*
  * Time loops on device buffers (hot-path loop row: sweeps and steps back to back on one
  * stream, as the benchmark workloads run them).
  *
@@ -193,8 +210,9 @@ int stencil_plan_host_phases(const stencil_plan* plan, float* ms, int n);
  * stencil_plan_launch_info) on a GPU with `num_sms` SMs that holds `ctas_per_sm` CTAs of
  * that kernel per SM.  Host-only: makes no CUDA call, so it also runs without a GPU
  * (capacity planning, tests).  Its cost does not grow with nz.  Writes to info[0..n):
- * grid CTAs, x-y tiles, z-chunks per tile column, work items, tile width, tile height
- * (all 0 but the tile sizes when the interior is empty).  Returns the number of values
+ * grid CTAs, x-y tiles, z-chunks per tile column, work items, tile width, tile height,
+ * x of the first tile column (0, or R where the kernel stores whole tiles through a map of
+ * the interior) (all 0 but the tile sizes and origin when the interior is empty).  Returns the number of values
  * written, or STENCIL_ERR_ARG for a grid or radius stencil_plan_create would reject, a
  * kind outside [0, 3], num_sms or ctas_per_sm < 1.
  */

@@ -61,6 +61,10 @@ def _load():
             lib.oracle_wave_step_f32.argtypes = [_I64, _I64, _I64, ctypes.c_int] + [_F32P] * 6
             lib.oracle_wave_points_f32.argtypes = [_I64, _I64, _I64, ctypes.c_int] + [_F32P] * 5 + \
                                                   [_I64, _I64P, _F32P]
+            lib.oracle_wave_step_eta7_f64.argtypes = [_I64, _I64, _I64, ctypes.c_int, _F64P, ctypes.c_double,
+                                                      ctypes.c_double] + [_F64P] * 5
+            lib.oracle_wave_step_eta7_f32.argtypes = [_I64, _I64, _I64, ctypes.c_int, _F32P, ctypes.c_float,
+                                                      ctypes.c_float] + [_F32P] * 5
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -159,6 +163,35 @@ def wave_step(u_prev, u, v2dt2, eta, coeffs, radius: int, u_next=None) -> np.nda
         c = _coeffs(coeffs, radius, np.float32)
         p = lambda a: _ptr(a, ctypes.c_float)  # noqa: E731
         lib.oracle_wave_step_f32(nx, ny, nz, radius, p(c), p(u_prev), p(u), p(u_next), p(v2dt2), p(eta))
+    else:
+        raise ValueError("float32 or float64 fields")
+    return u_next
+
+
+def wave_step_eta7(u_prev, u, v2dt2, eta, coeffs, radius: int, e0: float, e1: float, u_next=None):
+    """One acoustic step whose damping at a point is the radius-1 star stencil of eta,
+    e0*eta + e1*(its six face neighbours), in place of eta itself (see stencil_oracle.c).
+    Same conventions as wave_step."""
+    dt = u.dtype
+    for a in (u_prev, u, v2dt2, eta):
+        _check(a, dt, u.shape)
+    if u_next is None:
+        u_next = u_prev.copy()
+    _check(u_next, dt, u.shape)
+    if u_next is u:
+        raise ValueError("u_next must not be u")
+    nx, ny, nz = _grid(u)
+    lib = _load()
+    if dt == np.float64:
+        c = _coeffs(coeffs, radius, np.float64)
+        p = lambda a: _ptr(a, ctypes.c_double)  # noqa: E731
+        lib.oracle_wave_step_eta7_f64(nx, ny, nz, radius, p(c), float(e0), float(e1), p(u_prev), p(u),
+                                      p(u_next), p(v2dt2), p(eta))
+    elif dt == np.float32:
+        c = _coeffs(coeffs, radius, np.float32)
+        p = lambda a: _ptr(a, ctypes.c_float)  # noqa: E731
+        lib.oracle_wave_step_eta7_f32(nx, ny, nz, radius, p(c), float(e0), float(e1), p(u_prev), p(u),
+                                      p(u_next), p(v2dt2), p(eta))
     else:
         raise ValueError("float32 or float64 fields")
     return u_next

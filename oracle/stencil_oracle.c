@@ -195,3 +195,55 @@ void oracle_wave_points_f32(int64_t nx, int64_t ny, int64_t nz, int R, const flo
         vals[k] = wave_point_f32(u_prev, u, v2dt2, eta, i, sy, sz, R, c);
     }
 }
+
+/* ---- wave step with the damping read through a 7-point stencil of eta ------------ */
+
+/* "Accelerating High-Order Stencils on GPUs" says the computation on eta in the PML
+ * region is a low-order 7-point stencil (halo of eta: one point) but prints no formula.
+ * Reading: the damping at an interior point is the radius-1 star stencil of eta,
+ *   eff = e0*eta[i] + e1*(eta[i-1] + eta[i+1] + eta[i-nx] + eta[i+nx] + eta[i-nx*ny] + eta[i+nx*ny]),
+ * used in place of eta[i] in the update above.  With e0 + 6*e1 = 1 a constant eta gives
+ * back the pointwise update. */
+static double eta7_f64(const double* eta, int64_t i, int64_t sy, int64_t sz, double e0, double e1) {
+    double s = eta[i - 1] + eta[i + 1] + eta[i - sy] + eta[i + sy] + eta[i - sz] + eta[i + sz];
+    return e0 * eta[i] + e1 * s;
+}
+
+void oracle_wave_step_eta7_f64(int64_t nx, int64_t ny, int64_t nz, int R, const double* c,
+                               double e0, double e1, const double* u_prev, const double* u,
+                               double* u_next, const double* v2dt2, const double* eta) {
+    if (interior_empty(nx, ny, nz, R)) return;
+    const int64_t sy = nx, sz = nx * ny;
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t z = R; z < nz - R; ++z)
+        for (int64_t y = R; y < ny - R; ++y)
+            for (int64_t x = R; x < nx - R; ++x) {
+                int64_t i = x + sy * y + sz * z;
+                double lap = star_f64(u, i, 1, sy, sz, R, c);
+                double e = eta7_f64(eta, i, sy, sz, e0, e1);
+                double t = 2.0 * u[i] - (1.0 - e) * u_prev[i] + v2dt2[i] * lap;
+                u_next[i] = t / (1.0 + e);
+            }
+}
+
+void oracle_wave_step_eta7_f32(int64_t nx, int64_t ny, int64_t nz, int R, const float* cf,
+                               float e0f, float e1f, const float* u_prev, const float* u,
+                               float* u_next, const float* v2dt2, const float* eta) {
+    if (interior_empty(nx, ny, nz, R)) return;
+    double c[8];
+    for (int r = 0; r <= R; ++r) c[r] = (double)cf[r];
+    const double e0 = (double)e0f, e1 = (double)e1f;
+    const int64_t sy = nx, sz = nx * ny;
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t z = R; z < nz - R; ++z)
+        for (int64_t y = R; y < ny - R; ++y)
+            for (int64_t x = R; x < nx - R; ++x) {
+                int64_t i = x + sy * y + sz * z;
+                double lap = star_f32(u, i, 1, sy, sz, R, c);
+                double s = (double)eta[i - 1] + (double)eta[i + 1] + (double)eta[i - sy] +
+                           (double)eta[i + sy] + (double)eta[i - sz] + (double)eta[i + sz];
+                double e = e0 * (double)eta[i] + e1 * s;
+                double t = 2.0 * (double)u[i] - (1.0 - e) * (double)u_prev[i] + (double)v2dt2[i] * lap;
+                u_next[i] = (float)(t / (1.0 + e));
+            }
+}

@@ -68,6 +68,7 @@ def load():
         lib.wave_run_host.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
+        lib.wave_eta_stencil.argtypes = [vp, vp, vp, ctypes.c_float, ctypes.c_float, vp]
         lib.stencil_plan_host_phases.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         lib.stencil_schedule_query.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
@@ -84,7 +85,7 @@ def load():
         for fn in ("stencil_apply", "stencil_apply_semi", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
                    "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject",
-                   "stencil_schedule_query", "stencil_plan_host_phases", "stencil_slabs_extent",
+                   "stencil_schedule_query", "stencil_plan_host_phases", "wave_eta_stencil", "stencil_slabs_extent",
                    "stencil_slabs_exchange", "stencil_slabs_apply", "stencil_slabs_wave_step",
                    "stencil_slabs_status"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -185,6 +186,11 @@ class StencilPlan:
         _check(self._lib.wave_step_pml(self._p, *[_addr(f) for f in fields], int(pml_width),
                                        _stream(stream, *fields)))
 
+    def eta_stencil(self, eta, eta_eff, e0: float, e1: float, stream=None) -> None:
+        """wave_eta_stencil: eta_eff = e0*eta + e1*(six face neighbours), once per model."""
+        _check(self._lib.wave_eta_stencil(self._p, _addr(eta), _addr(eta_eff), float(e0), float(e1),
+                                          _stream(stream, eta, eta_eff)))
+
     def sweeps(self, a, b, nsweeps: int, use_graph: bool = False, stream=None) -> None:
         """stencil_sweeps: ping-pong sweeps a -> b -> a ...; odd counts end in b."""
         _check(self._lib.stencil_sweeps(self._p, _addr(a), _addr(b), int(nsweeps), int(use_graph),
@@ -284,7 +290,7 @@ class StencilSlabs:
             pass
 
 
-SCHEDULE_KEYS = ("grid", "tiles", "zchunks", "items", "tile_x", "tile_y")
+SCHEDULE_KEYS = ("grid", "tiles", "zchunks", "items", "tile_x", "tile_y", "x_origin")
 
 
 def schedule_query(nx: int, ny: int, nz: int, radius: int, kind: int, num_sms: int,

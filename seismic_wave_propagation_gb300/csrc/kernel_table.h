@@ -10,7 +10,7 @@ namespace libstencil {
 
 using LaunchFn = cudaError_t (*)(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                                  const CUtensorMap& uprev, const CUtensorMap& v2dt2,
-                                 const CUtensorMap& eta, const StarParams& p);
+                                 const CUtensorMap& eta, const CUtensorMap& out, const StarParams& p);
 
 struct KernelDesc {
   const void* fn;   // kernel entry (for attributes and occupancy)
@@ -19,32 +19,35 @@ struct KernelDesc {
   int tile_y;       // output tile height (width is kTX)
   int stages;       // u ring slots
   int box_w, box_h; // u box (floats)
+  bool tstore;      // output stored by TMA through a map of the interior (tiles start at x = R)
   LaunchFn launch;
 };
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false, bool DRIFT = false>
+          bool PML = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
-                        const StarParams& p) {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
-  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>
-      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, p);
+                        const CUtensorMap& out, const StarParams& p) {
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
+  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>
+      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, out, p);
   return cudaGetLastError();
 }
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false, bool DRIFT = false>
+          bool PML = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
 KernelDesc make_desc() {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
-  return KernelDesc{(const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>,
-                    C::kThreads,
-                    C::kSmemBytes,
-                    C::TY,
-                    STAGES,
-                    C::BW,
-                    C::BH,
-                    &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT>};
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
+  return KernelDesc{
+      (const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>,
+      C::kThreads,
+      C::kSmemBytes,
+      C::TY,
+      STAGES,
+      C::BW,
+      C::BH,
+      TSTORE,
+      &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>};
 }
 
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `pml`: the wave step

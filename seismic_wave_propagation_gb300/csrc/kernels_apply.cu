@@ -14,7 +14,7 @@ KernelDesc apply_kernel_desc(int radius) {
     case 1: return make_desc<1, 2, 16, 5, 1, false, 1, 1, false, false, true>();
     case 2: return make_desc<2, 2, 16, 6, 1, false, 1, 1, false, false, true>();
     case 3: return make_desc<3, 2, 16, 7, 1, false, 1, 1, false, false, true>();
-    default: return make_desc<4, 2, 16, 5, 1, false, 2, 2>();
+    default: return make_desc<4, 2, 16, 5, 1, false, 2, 2, false, false, false, true>();
   }
 }
 

@@ -54,6 +54,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapEntry {
   const void* ptr = nullptr;
   int box_w = 0, box_h = 0;
+  int view = 0;  // 0: the whole grid; 1: its interior (points at least R from every face)
   uint64_t stamp = 0;
   CUtensorMap map;
 };
@@ -86,6 +87,7 @@ struct stencil_plan {
   cudaEvent_t ev[2 * 32 + 2];
   bool pipe_ready;
   int pipe_slabs;        // slabs of the last pipelined call (0: none yet)
+  stencil_plan* eta_plan;  // radius-1 plan of the same grid for wave_eta_stencil (on first use)
 };
 
 namespace {
@@ -114,9 +116,11 @@ struct Schedule {
 constexpr int64_t kMaxRounds = 1 << 14;
 
 Schedule schedule(int64_t nx, int64_t ny, int R, int tile_y, int kind, int num_sms, int occupancy,
-                  int nzi) {
+                  int nzi, bool interior_tiles) {
   Schedule sc{};
-  sc.ntx = (int)((nx + kTX - 1) / kTX);
+  // Tiles cover x from 0 (masked stores), or from the interior origin R (TMA stores).
+  const int64_t xext = interior_tiles ? nx - 2 * R : nx;
+  sc.ntx = (int)((xext + kTX - 1) / kTX);
   const int nty = (int)((ny - 2 * R + tile_y - 1) / tile_y);
   sc.ntiles = sc.ntx * nty;
   const int64_t slots = (int64_t)num_sms * std::max(1, occupancy);
@@ -186,7 +190,8 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
     grid = 0;
     return;
   }
-  const Schedule sc = schedule(p->nx, p->ny, R, kd.tile_y, kind, p->num_sms, p->occupancy[kind], nzi);
+  const Schedule sc =
+      schedule(p->nx, p->ny, R, kd.tile_y, kind, p->num_sms, p->occupancy[kind], nzi, kd.tstore);
   sp.ntx = sc.ntx;
   sp.ntiles = sc.ntiles;
   sp.nzi = nzi;
@@ -232,11 +237,14 @@ bool overlap(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
-// TMA descriptor for a field pointer and box shape (cached per plan).
-int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtensorMap** out) {
+// TMA descriptor for a field pointer and box shape (cached per plan).  view 1 maps the
+// interior only: its origin is the point (R, R, R), so a box stored through it never writes
+// the shell (the TMA unit drops the parts of a box outside the tensor).
+int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtensorMap** out,
+            int view = 0) {
   MapEntry* victim = &p->maps[0];
   for (MapEntry& m : p->maps) {
-    if (m.ptr == ptr && m.box_w == box_w && m.box_h == box_h) {
+    if (m.ptr == ptr && m.box_w == box_w && m.box_h == box_h && m.view == view) {
       m.stamp = ++p->clock;
       *out = &m.map;
       return STENCIL_OK;
@@ -245,11 +253,16 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   }
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail(STENCIL_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const cuuint64_t dims[3] = {(cuuint64_t)p->nx, (cuuint64_t)p->ny, (cuuint64_t)p->nz};
+  const int64_t e = view ? 2 * p->radius : 0;
+  const cuuint64_t dims[3] = {(cuuint64_t)(p->nx - e), (cuuint64_t)(p->ny - e), (cuuint64_t)(p->nz - e)};
   const cuuint64_t strides[2] = {(cuuint64_t)p->nx * 4, (cuuint64_t)(p->nx * p->ny) * 4};
   const cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims,
+  const int64_t org = view ? p->radius * (1 + p->nx + p->nx * p->ny) : 0;  // floats to (R, R, R)
+  void* gbase = const_cast<float*>(static_cast<const float*>(ptr)) + org;
+  if (reinterpret_cast<uintptr_t>(gbase) & 15u)
+    return fail(STENCIL_ERR_ALIGNMENT, "interior origin of the output is not 16-byte aligned");
+  CUresult r = enc(&victim->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, gbase, dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -260,6 +273,7 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   victim->ptr = ptr;
   victim->box_w = box_w;
   victim->box_h = box_h;
+  victim->view = view;
   victim->stamp = ++p->clock;
   *out = &victim->map;
   return STENCIL_OK;
@@ -285,12 +299,14 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   } else {
     mp = mv = me = mu;
   }
+  const CUtensorMap* mo = mu;
+  if (kd.tstore && (rc = get_map(p, out, kTX, kd.tile_y, &mo, 1))) return rc;
   sp.out = out;
   sp.pml = pml;
   sp.debug_skip = p->debug_mode == 1 ? 0 : -1;  // every CTA has a load 0
   // Copy the descriptors: the cache may evict entries while the launch is pending.
-  const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me;
-  cudaError_t e = kd.launch(dim3(grid), stream, a, b, c, d, sp);
+  const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me, o = *mo;
+  cudaError_t e = kd.launch(dim3(grid), stream, a, b, c, d, o, sp);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return STENCIL_OK;
 }
@@ -473,6 +489,7 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
 
 void stencil_plan_destroy(stencil_plan* p) {
   if (!p) return;
+  if (p->eta_plan) stencil_plan_destroy(p->eta_plan);
   if (p->graph) cudaGraphExecDestroy(p->graph);
   if (p->pipe_ready) {
     for (cudaStream_t q : p->pipe) cudaStreamDestroy(q);
@@ -537,6 +554,30 @@ int wave_step_pml(stencil_plan* p, const float* u_prev, const float* u, float* u
     return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
   const int pml = (int)std::min<int64_t>(pml_width, 1 << 30);
   return launch(p, 2, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream), pml);
+}
+
+int wave_eta_stencil(stencil_plan* p, const float* eta, float* eta_eff, float e0, float e1, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, eta, "eta")) || (rc = check_field(p, eta_eff, "eta_eff"))) return rc;
+  const size_t bytes = (size_t)npoints(p) * 4;
+  if (overlap(eta, eta_eff, bytes)) return fail(STENCIL_ERR_ALIAS, "eta and eta_eff overlap");
+  if (!p->eta_plan) {
+    const float c[2] = {e0, e1};
+    p->eta_plan = stencil_plan_create(p->nx, p->ny, p->nz, 1, c);
+    if (!p->eta_plan) return STENCIL_ERR_CUDA;
+  }
+  stencil_plan* q = p->eta_plan;
+  if (q->c[0] != e0 || q->c[1] != e1) {  // new weights: the launch parameters carry them
+    q->c[0] = e0;
+    q->c[1] = e1;
+    for (int k = 0; k < 4; ++k) plan_geometry(q, k);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(eta_eff, eta, bytes, cudaMemcpyDeviceToDevice, s);  // the faces
+  if (e != cudaSuccess) return cuda_fail(e, "eta copy");
+  return launch(q, 0, eta, nullptr, nullptr, nullptr, eta_eff, s);
 }
 
 int stencil_sweeps(stencil_plan* p, float* a, float* b, int nsweeps, int use_graph, void* stream) {
@@ -604,6 +645,7 @@ int stencil_plan_status(stencil_plan* p, void* stream) {
   if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
   int rc = check_device(p);
   if (rc) return rc;
+  if (p->eta_plan && (rc = stencil_plan_status(p->eta_plan, stream))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned h[4] = {0, 0, 0, 0};
   cudaError_t e = cudaStreamSynchronize(s);
@@ -717,9 +759,9 @@ int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int k
   const int64_t m = 2 * (int64_t)radius + 1;
   Schedule sc{};
   if (nx >= m && ny >= m && nz >= m)
-    sc = schedule(nx, ny, radius, kd.tile_y, kind, num_sms, ctas_per_sm, (int)(nz - 2 * radius));
-  const int64_t v[6] = {sc.grid, sc.ntiles, sc.nchunks, sc.nitems, kTX, kd.tile_y};
-  const int k = std::min(n, 6);
+    sc = schedule(nx, ny, radius, kd.tile_y, kind, num_sms, ctas_per_sm, (int)(nz - 2 * radius), kd.tstore);
+  const int64_t v[7] = {sc.grid, sc.ntiles, sc.nchunks, sc.nitems, kTX, kd.tile_y, kd.tstore ? radius : 0};
+  const int k = std::min(n, 7);
   for (int i = 0; i < k; ++i) info[i] = v[i];
   return k;
 }

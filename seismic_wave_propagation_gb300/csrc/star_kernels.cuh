@@ -69,10 +69,11 @@ struct StarParams {
 // Producer cursor: the next load of the CTA's sequence (kept in shared memory; the warps
 // that refill the ring take turns, and the CTA barrier between turns orders them).
 struct Cursor {
-  int item, j, L, x0, y0, za, issued, pad;
+  int item, j, L, x0, y0, zs, issued, dz;  // plane landed at step j: zs + dz * j
 };
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, bool SEMI = false>
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, bool SEMI = false,
+          bool TSTORE = false, int KB = 1>
 struct StarCfg {
   static constexpr int kThreads = kThreadsX * NWY;
   static constexpr int TY = TYT * NWY;  // output tile height
@@ -88,13 +89,20 @@ struct StarCfg {
   static constexpr int kIssOff = kCntOff + 4 * kNumBars;                // last load per slot
   static constexpr int kRingOffset = (kIssOff + 4 * kNumBars + 127) / 128 * 128;
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
-  static constexpr int kSmemBytes = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
+  static constexpr int kStgOffset = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
+  static constexpr int kStgPlaneBytes = kTX * TY * 4;  // one output tile, staged for a TMA store
+  static constexpr int kStgPlanes = TSTORE ? 2 * KB : 0;
+  static constexpr int kSmemBytes = kStgOffset + kStgPlanes * kStgPlaneBytes;
+  static constexpr int XO = TSTORE ? R : 0;  // x of the first tile's first output
   static constexpr int KEEP = (WAVE || SEMI) ? R : 0;   // planes kept behind the lead
   static constexpr int kLookahead = STAGES - KEEP - 1;  // planes in flight beyond the lead
   static_assert(kLookahead >= 1, "ring must hold the kept planes plus one in flight");
   static_assert(BW <= 256 && BH <= 256, "TMA box dimensions are limited to 256");
   static_assert((BW * 4) % 16 == 0, "TMA inner box bytes must be a multiple of 16");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  // TMA-stored tiles start at the interior origin x = R; the staged input box then starts
+  // at x = R - kHX, which must be 0 for its x coordinate to stay 16-byte aligned.
+  static_assert(!TSTORE || R == kHX, "TMA stores of the output need R == 4");
 };
 
 // ---- PTX wrappers ------------------------------------------------------------------
@@ -163,6 +171,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bulk tensor store of a staged tile (shared -> global through the TMA unit), tracked in
+// the issuing thread's bulk groups.  Parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The issuing thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// The issuing thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float4 lds4(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
@@ -201,17 +229,24 @@ __device__ __forceinline__ float get(const float4& v, int e) {
 
 // ---- work decomposition -------------------------------------------------------------
 
-template <int R, int TY>
+// Item -> output tile (x0, y0), its L = zb - za + 2R landed planes and their order: the
+// plane landed at step j is zs + dz * j, the output plane completed at step j >= 2R is
+// zs + dz * (j - R).  Every chunk marches up (dz = 1) from za - R; the z filter is
+// symmetric, so a chunk marching down from zb + R - 1 (dz = -1) would compute the same.
+template <int R, int TY, int XO>
 __device__ __forceinline__ void item_geometry(const StarParams& p, int item, int& x0, int& y0,
-                                              int& za, int& zb) {
+                                              int& L, int& zs, int& dz) {
   const int chunk = item / p.ntiles;
   const int tile = item - chunk * p.ntiles;
   const int by = tile / p.ntx;
   const int bx = tile - by * p.ntx;
-  x0 = bx * kTX;
+  x0 = XO + bx * kTX;
   y0 = R + by * TY;
-  za = R + p.zoff + (int)(((long long)chunk * p.nzi) / p.nchunks);
-  zb = R + p.zoff + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
+  const int za = R + p.zoff + (int)(((long long)chunk * p.nzi) / p.nchunks);
+  const int zb = R + p.zoff + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
+  L = zb - za + 2 * R;
+  dz = 1;
+  zs = za - R;
 }
 
 // Does the wave step need eta for the output tile at (x0, y0), plane z?  Only where the
@@ -222,41 +257,37 @@ __device__ __forceinline__ bool tile_needs_eta(const StarParams& p, int x0, int 
          y0 + TY > p.ny - p.pml;
 }
 
-template <int R, int TY>
+template <int R, int TY, int XO>
 __device__ __forceinline__ void cursor_set_item(const StarParams& p, Cursor& k, int item) {
   k.item = item;
   k.j = 0;
-  if (item < p.nitems) {
-    int x0, y0, za, zb;
-    item_geometry<R, TY>(p, item, x0, y0, za, zb);
-    k.x0 = x0;
-    k.y0 = y0;
-    k.za = za;
-    k.L = zb - za + 2 * R;
-  }
+  if (item < p.nitems) item_geometry<R, TY, XO>(p, item, k.x0, k.y0, k.L, k.zs, k.dz);
 }
 
-template <int R, int TY>
+template <int R, int TY, int XO>
 __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
-  if (++k.j == k.L) cursor_set_item<R, TY>(p, k, k.item + (int)gridDim.x);
+  if (++k.j == k.L) cursor_set_item<R, TY, XO>(p, k, k.item + (int)gridDim.x);
 }
 
 // ---- the kernel ----------------------------------------------------------------------
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML,
-          bool SEMI, bool DRIFT>
+          bool SEMI, bool DRIFT, bool TSTORE>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
                       const __grid_constant__ CUtensorMap tm_v2dt2,
-                      const __grid_constant__ CUtensorMap tm_eta, const __grid_constant__ StarParams p) {
-  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI>;
+                      const __grid_constant__ CUtensorMap tm_eta,
+                      const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ StarParams p) {
+  using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
+  static_assert(!(TSTORE && (SEMI || DRIFT)), "TMA stores: plain sweep or wave step, barrier protocol");
   static_assert(!(WAVE && SEMI), "the semi-stencil form is a plain sweep");
   static_assert(!(WAVE && DRIFT), "the wave step's aux ring needs the per-plane barrier");
   constexpr int TY = C::TY;
   constexpr int BW = C::BW;
   constexpr int KEEP = C::KEEP;
   constexpr int PSTRIDE = C::kPlaneStride / 4;  // floats between ring slots
+  constexpr int XO = C::XO;
 
   extern __shared__ __align__(128) unsigned char smem[];
   Cursor* cur = reinterpret_cast<Cursor*>(smem + C::kCurOff);  // [0] u loads, [1] aux loads
@@ -267,6 +298,8 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   const uint32_t aux_base = base + C::kAuxOffset;
   const float* ring = reinterpret_cast<const float*>(smem + C::kRingOffset);
   const float* auxr = reinterpret_cast<const float*>(smem + C::kAuxOffset);
+  float* stg = reinterpret_cast<float*>(smem + C::kStgOffset);  // staged output tiles (TSTORE)
+  const uint32_t stg_base = base + C::kStgOffset;
 
   if ((int)blockIdx.x >= p.nitems) return;
 
@@ -289,10 +322,10 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     if (counter != p.debug_skip) {
       mbar_arrive_expect_tx(bar, C::kPlaneBytes);
       tma_load_3d(ring_base + slot * C::kPlaneStride, &tm_u, bar, k.x0 - kHX, k.y0 - R,
-                  k.za - R + k.j);
+                  k.zs + k.dz * k.j);
     }
     ++k.issued;
-    cursor_advance<R, TY>(p, k);
+    cursor_advance<R, TY, XO>(p, k);
   };
   // Producer: stage u_prev, v2dt2, eta of the output plane of an emitting step.
   auto produce_aux = [&](int counter) {
@@ -302,7 +335,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     const uint32_t bar = base + 8u * (STAGES + slot);
     if (k.j >= 2 * R) {
       const uint32_t dst = aux_base + slot * C::kAuxStageBytes;
-      const int z = k.za + k.j - 2 * R;
+      const int z = k.zs + k.dz * (k.j - R);
       const bool eta = !PML || tile_needs_eta<TY>(p, k.x0, k.y0, z);
       mbar_arrive_expect_tx(bar, (eta ? 3 : 2) * C::kAuxFieldBytes);
       tma_load_3d(dst, &tm_uprev, bar, k.x0, k.y0, z);
@@ -312,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
       mbar_arrive(bar);  // filling step: nothing to stage, just complete the phase
     }
     ++k.issued;
-    cursor_advance<R, TY>(p, k);
+    cursor_advance<R, TY, XO>(p, k);
   };
 
   const bool bad_smem = (base & 127u) != 0u;  // TMA destinations need 128-B alignment
@@ -324,7 +357,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
       lastld[s] = -1;
     }
     fence_mbar_init();
-    cursor_set_item<R, TY>(p, cur[0], blockIdx.x);
+    cursor_set_item<R, TY, XO>(p, cur[0], blockIdx.x);
     cur[0].issued = 0;
     cur[1] = cur[0];
   }
@@ -363,11 +396,12 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
   uint32_t aphase = 0;     // (J / ASTAGES) & 1
   int pwarp = 0;           // the warp that refills the ring at the next barrier
   int since = 0;           // steps since the last CTA barrier (one barrier per KB planes)
+  int stg_slot = 0;        // staging tile of the next output plane (TSTORE)
+  int emitted = 0;         // output planes staged since the last barrier (TSTORE)
   const size_t plane = (size_t)p.nx * p.ny;
   for (int item = blockIdx.x; item < p.nitems; item += gridDim.x) {
-    int x0, y0, za, zb;
-    item_geometry<R, TY>(p, item, x0, y0, za, zb);
-    const int L = zb - za + 2 * R;  // planes za-R .. zb+R-1 land in turn
+    int x0, y0, L, zs, dz;
+    item_geometry<R, TY, XO>(p, item, x0, y0, L, zs, dz);  // L planes land in turn
     const int gx = x0 + col;
     const int gy0 = y0 + row0;
     // Output masks and row addresses of this thread, fixed for the whole item.
@@ -385,7 +419,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
 
       if (j >= 2 * R) {
         // Output plane z = (landed plane) - R is complete once its z part is added.
-        const int z = za + j - 2 * R;
+        const int z = zs + dz * (j - R);
         P4 o[TYT];
 #pragma unroll
         for (int k = 0; k < TYT; ++k) o[k] = fma2x(cc[R], xv[k], s[0][k]);
@@ -424,17 +458,27 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
             }
           }
         }
-        float* const oz = orow + (size_t)z * plane;
+        if constexpr (TSTORE) {
+          // Stage the tile; after the next CTA barrier one thread stores it with TMA, which
+          // writes only the part inside the interior (the tiles start at its origin).
+          float* st = stg + stg_slot * (C::kStgPlaneBytes / 4) + row0 * kTX + col;
 #pragma unroll
-        for (int k = 0; k < TYT; ++k) {
-          if (row_ok[k]) {
-            float* dst = oz + k * p.nx;
-            if (vec_ok) {
-              __stcs(reinterpret_cast<float4*>(dst), tof4(o[k]));
-            } else {
+          for (int k = 0; k < TYT; ++k) *reinterpret_cast<float4*>(st + k * kTX) = tof4(o[k]);
+          if (++stg_slot == C::kStgPlanes) stg_slot = 0;
+          ++emitted;
+        } else {
+          float* const oz = orow + (size_t)z * plane;
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (gx + e >= R && gx + e < p.nx - R) dst[e] = pget(o[k], e);
+          for (int k = 0; k < TYT; ++k) {
+            if (row_ok[k]) {
+              float* dst = oz + k * p.nx;
+              if (vec_ok) {
+                __stcs(reinterpret_cast<float4*>(dst), tof4(o[k]));
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (gx + e >= R && gx + e < p.nx - R) dst[e] = pget(o[k], e);
+              }
             }
           }
         }
@@ -549,15 +593,11 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         __syncwarp();
         if (lane0 && atomicAdd(&relcnt[rslot], 1) == NWARPS - 1) {
           relcnt[rslot] = 0;  // published to the next round by the refill's arrive (release)
-          int jj = j + STAGES - KEEP, it = item, L2 = L, nx0 = x0, ny0 = y0, nza = za;
+          int jj = j + STAGES - KEEP, it = item, L2 = L, nx0 = x0, ny0 = y0, nzs = zs, ndz = dz;
           while (jj >= L2 && it < p.nitems) {
             jj -= L2;
             it += (int)gridDim.x;
-            if (it < p.nitems) {
-              int zb2;
-              item_geometry<R, TY>(p, it, nx0, ny0, nza, zb2);
-              L2 = zb2 - nza + 2 * R;
-            }
+            if (it < p.nitems) item_geometry<R, TY, XO>(p, it, nx0, ny0, L2, nzs, ndz);
           }
           if (it < p.nitems) {
             const int counter = J - 1 + STAGES - KEEP;
@@ -567,7 +607,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
             if (counter != p.debug_skip) {
               mbar_arrive_expect_tx(bar, C::kPlaneBytes);
               tma_load_3d(ring_base + rslot * C::kPlaneStride, &tm_u, bar, nx0 - kHX, ny0 - R,
-                          nza - R + jj);
+                          nzs + ndz * jj);
             }
           }
         }
@@ -586,7 +626,26 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
         aphase ^= 1u;
       }
       if (++since < KB && j + 1 < L) continue;
+      if constexpr (TSTORE) {
+        fence_proxy_async_smem();  // this thread's staged tiles become visible to the TMA unit
+        // The stores issued at the previous barrier have read their staging tiles, which
+        // the steps after this barrier may overwrite (2*KB tiles, at most KB per interval).
+        if (leader) bulk_wait_read_all();
+      }
       const bool stop = __syncthreads_or(failed) != 0;
+      if constexpr (TSTORE) {
+        if (leader && !stop && emitted > 0) {
+          // The planes staged since the last barrier are the last `emitted` steps'.
+          for (int q = 0; q < emitted; ++q) {
+            const int z = zs + dz * (j - emitted + 1 + q - R);
+            int sl = stg_slot - emitted + q;
+            if (sl < 0) sl += C::kStgPlanes;
+            tma_store_3d(&tm_out, stg_base + sl * C::kStgPlaneBytes, x0 - R, y0 - R, z - R);
+          }
+          bulk_commit();
+        }
+        emitted = 0;
+      }
       if (lane0 && !stop) {
         if (warp == pwarp) {
           fence_proxy_async_smem();
@@ -607,6 +666,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     // The warps leave the loops at different times; they meet here to decide together.
     if (__syncthreads_or(failed)) goto drain;
   }
+  if (TSTORE && leader) bulk_wait_all();  // the last tiles are written before the CTA leaves
   return;
 
 drain:
@@ -614,6 +674,7 @@ drain:
   // memory before the CTA exits (bounded as well), then leave.
   // Only the last load issued into each slot can still be outstanding.
   if (leader) {
+    if (TSTORE) bulk_wait_all();
     for (int sl = 0; sl < STAGES; ++sl) {
       const int c = lastld[sl];
       if (c >= 0 && c != p.debug_skip && !mbar_wait_bounded(base + 8u * sl, (c / STAGES) & 1))

@@ -242,3 +242,58 @@ def test_native_step_loop_matches_step_by_step(use_graph, pml):
     assert torch.equal(bufs[(steps + 1) % 3], b)
     assert torch.equal(bufs[steps % 3], a)
     plan.close()
+
+
+def test_eta_stencil_damping_field_matches_oracle():
+    """wave_eta_stencil: the radius-1 star stencil of eta everywhere but on the faces, which
+    keep eta's values; new weights on a second call take effect."""
+    torch = torch_cuda()
+    nx, ny, nz = 136, 75, 41
+    e = synth.uniform_field(nx, ny, nz, seed=61, scale=0.05) + np.float32(0.05)
+    plan = StencilPlan(nx, ny, nz, 4, synth.laplacian8_coeffs())
+    d = torch.from_numpy(e.ravel()).cuda()
+    out = torch.full_like(d, 9.0)
+    for e0, e1 in ((0.5, 1.0 / 12.0), (0.25, 0.125)):
+        plan.eta_stencil(d, out, e0, e1)
+        plan.status(None, out)
+        got = out.cpu().numpy().reshape(e.shape)
+        want = oracle.apply(e, np.float32([e0, e1]), 1)  # faces copied from e
+        m1 = interior_mask(e.shape, 1)
+        assert np.max(np.abs(got[m1].astype(np.float64) - want[m1])) <= 1e-6 * 0.1
+        np.testing.assert_array_equal(got[~m1], e[~m1])
+    plan.close()
+
+
+@pytest.mark.parametrize("nsteps,dims", [(1, (136, 75, 41)), (25, (96, 80, 72))])
+def test_wave_with_7_point_eta_stencil_matches_oracle(nsteps, dims):
+    """The PML step whose damping is the 7-point stencil of eta: wave_eta_stencil once, then
+    wave_steps (one CUDA graph) on the result, against the oracle's direct 7-point step."""
+    torch = torch_cuda()
+    nx, ny, nz = dims
+    c = synth.laplacian8_coeffs()
+    c32 = c.astype(np.float32)
+    e0, e1 = 0.5, 1.0 / 12.0
+    up, u, s, _ = synth.wave_fields(nx, ny, nz)
+    u = (u + synth.uniform_field(nx, ny, nz, seed=62, scale=0.01)).astype(np.float32)
+    e = synth.sponge_eta(nx, ny, nz, width=10) + synth.uniform_field(nx, ny, nz, seed=63, scale=0.01) + \
+        np.float32(0.01)
+    e = e.astype(np.float32)
+    plan = StencilPlan(nx, ny, nz, 4, c)
+    f = [torch.from_numpy(x.ravel()).cuda() for x in (up, u, s, e)]
+    eff = torch.empty_like(f[3])
+    plan.eta_stencil(f[3], eff, e0, e1)
+    bufs = [f[0], f[1], f[0].clone()]
+    plan.wave_steps(bufs[0], bufs[1], bufs[2], f[2], eff, nsteps, use_graph=True)
+    plan.status(None, bufs[0])
+    got = bufs[(nsteps + 1) % 3].cpu().numpy().reshape(u.shape)
+    a, b, t = up.copy(), u.copy(), up.copy()
+    for _ in range(nsteps):
+        oracle.wave_step_eta7(a, b, s, e, c32, 4, e0, e1, u_next=t)
+        a, b, t = b, t, a
+    m = interior_mask(u.shape, 4)
+    if nsteps == 1:
+        assert np.max(np.abs(got[m] - b[m])) <= 1e-5 * (2 + 0.2025 * 19.51) * float(np.max(np.abs(u)))
+    else:
+        assert rel_l2(got, b) <= 1e-5
+    np.testing.assert_array_equal(got[~m], b[~m])
+    plan.close()

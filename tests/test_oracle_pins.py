@@ -393,6 +393,61 @@ def test_run_wave_zero_and_one_step(oracle_mod):
     np.testing.assert_array_equal(b, oracle_mod.wave_step(up, u, s, e, LAP8, 4))
 
 
+def test_eta7_constant_eta_gives_the_pointwise_step(oracle_mod):
+    """Weights with e0 + 6 e1 = 1 (the register-rotation lab's 1/4 and 1/8, exact in binary)
+    keep a constant eta unchanged, so the step equals the pointwise one bit for bit."""
+    shape = (14, 13, 15)
+    up = rng(41).uniform(-1, 1, shape)
+    u = rng(42).uniform(-1, 1, shape)
+    s = rng(43).uniform(0, 0.2, shape)
+    K = np.full(shape, 0.0625)
+    a = oracle_mod.wave_step_eta7(up, u, s, K, LAP8, 4, 0.25, 0.125)
+    b = oracle_mod.wave_step(up, u, s, K, LAP8, 4)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_eta7_centre_weight_alone_is_the_pointwise_step(oracle_mod):
+    shape = (13, 14, 12)
+    up, u = rng(44).uniform(-1, 1, shape), rng(45).uniform(-1, 1, shape)
+    s, e = rng(46).uniform(0, 0.2, shape), rng(47).uniform(0, 0.1, shape)
+    np.testing.assert_array_equal(oracle_mod.wave_step_eta7(up, u, s, e, LAP8, 4, 1.0, 0.0),
+                                  oracle_mod.wave_step(up, u, s, e, LAP8, 4))
+
+
+def test_eta7_brute_force(oracle_mod):
+    """Every interior point of a small grid from an explicit neighbour list."""
+    shape = (10, 11, 9)
+    up, u = rng(48).standard_normal(shape), rng(49).standard_normal(shape)
+    s, e = rng(50).uniform(0, 0.2, shape), rng(51).uniform(0, 0.1, shape)
+    c = [-6.0, 1.0]
+    e0, e1 = 0.3, 0.07
+    got = oracle_mod.wave_step_eta7(up, u, s, e, c, 1, e0, e1, u_next=np.zeros(shape))
+    nbrs = [(1, 0, 0), (-1, 0, 0), (0, 1, 0), (0, -1, 0), (0, 0, 1), (0, 0, -1)]
+    for z in range(1, shape[0] - 1):
+        for y in range(1, shape[1] - 1):
+            for x in range(1, shape[2] - 1):
+                lap = c[0] * u[z, y, x] + c[1] * sum(u[z + a, y + b, x + d] for a, b, d in nbrs)
+                eff = e0 * e[z, y, x] + e1 * sum(e[z + a, y + b, x + d] for a, b, d in nbrs)
+                want = (2 * u[z, y, x] - (1 - eff) * up[z, y, x] + s[z, y, x] * lap) / (1 + eff)
+                assert abs(got[z, y, x] - want) < 1e-13
+
+
+def test_eta7_equals_the_pointwise_step_on_the_smoothed_damping(oracle_mod):
+    """Since eta does not change in time, the step is the pointwise step on the damping field
+    e0*eta + e1*(six neighbours), which the (pinned) radius-1 stencil computes."""
+    shape = (16, 15, 17)
+    up, u = rng(52).standard_normal(shape), rng(53).standard_normal(shape)
+    s, e = rng(54).uniform(0, 0.2, shape), rng(55).uniform(0, 0.1, shape)
+    eff = oracle_mod.apply(e, [0.5, 1.0 / 12.0], 1)
+    np.testing.assert_allclose(oracle_mod.wave_step_eta7(up, u, s, e, LAP8, 4, 0.5, 1.0 / 12.0),
+                               oracle_mod.wave_step(up, u, s, eff, LAP8, 4), rtol=0, atol=1e-14)
+    f = [x.astype(np.float32) for x in (up, u, s, e)]
+    eff32 = oracle_mod.apply(f[3], np.float32([0.5, 1.0 / 12.0]), 1)
+    a = oracle_mod.wave_step_eta7(f[0], f[1], f[2], f[3], LAP8.astype(np.float32), 4, 0.5, 1.0 / 12.0)
+    b = oracle_mod.wave_step(f[0], f[1], f[2], eff32, LAP8.astype(np.float32), 4)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-6)
+
+
 def test_sweeps_keep_a_fixed_shell(oracle_mod):
     u0 = rng(19).uniform(-1, 1, (10, 11, 12)).astype(np.float32)
     out = oracle_mod.run_sweeps(u0, LAP2.astype(np.float32), 1, 3)

@@ -23,10 +23,11 @@ def lib():
     return _lib.load()
 
 
-def full_scan(nx, ny, nz, R, tile_y, kind, sms, occ):
-    """Every chunk count from 1 to nzi, scored as the planner scores them."""
+def full_scan(nx, ny, nz, R, tile_y, kind, sms, occ, x_origin=0):
+    """Every chunk count from 1 to nzi, scored as the planner scores them (tiles cover x
+    from 0, or from the interior origin x = R)."""
     nzi = nz - 2 * R
-    ntiles = math.ceil(nx / TILE_X) * math.ceil((ny - 2 * R) / tile_y)
+    ntiles = math.ceil((nx - 2 * x_origin) / TILE_X) * math.ceil((ny - 2 * R) / tile_y)
     slots = sms * occ
 
     def score(n):
@@ -58,7 +59,8 @@ SHAPES = [(512, 512, 512), (640, 640, 640), (1536, 1536, 256), (64, 64, 64), (13
 def test_choice_matches_a_scan_over_every_chunk_count(nx, ny, nz, R, kind, occ, sms):
     got = _lib.schedule_query(nx, ny, nz, R, kind, sms, occ)
     tile_y = got["tile_y"]
-    ntiles, pick = full_scan(nx, ny, nz, R, tile_y, kind, sms, occ)
+    assert got["x_origin"] in (0, R)
+    ntiles, pick = full_scan(nx, ny, nz, R, tile_y, kind, sms, occ, got["x_origin"])
     assert got["tiles"] == ntiles
     assert got["zchunks"] == pick
     assert got["items"] == ntiles * pick
