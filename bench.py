@@ -497,6 +497,64 @@ def _first_step_parity(torch, plan, w, c, stream, samples=40000):
     return float(np.max(np.abs(got.astype(np.float64) - want))) / tol
 
 
+def run_extra_rows(torch, stream, peak):
+    """The next rows beside the workloads: the wave step on the 7-point eta damping (its
+    one-off damping pass and a step on the result), the region-split step, and the 512^3
+    25-point sweep held as z-slabs with its ghost exchange (one GPU)."""
+    from seismic_wave_propagation_gb300 import StencilPlan, StencilSlabs
+    out = {}
+    n = 640
+    c = synth.laplacian8_coeffs()
+    plan = StencilPlan(n, n, n, R, c)
+    f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(n, n, n)]
+    eff = torch.empty_like(f[3])
+    nxt = f[0].clone()
+    with torch.cuda.stream(stream):
+        ms_eta = _time_loop(lambda: plan.eta_stencil(f[3], eff, 0.5, 1.0 / 12.0, stream), 20, 3, stream)
+        ms_plain = _time_loop(lambda: plan.wave_step(f[0], f[1], nxt, f[2], f[3], stream), 30, 3, stream)
+        ms_eff = _time_loop(lambda: plan.wave_step(f[0], f[1], nxt, f[2], eff, stream), 30, 3, stream)
+        ms_pml = _time_loop(lambda: plan.wave_step_pml(f[0], f[1], nxt, f[2], f[3], 16, stream), 30, 3, stream)
+        plan.status(stream)
+    wb = traffic.wave_bytes(n, n, n, R)
+    out["wave 640^3, pointwise eta"] = json.dumps({"ms": round(ms_plain, 4), "frac_of_peak": round(wb / (ms_plain / 1e3) / 1e9 / peak, 3)})
+    out["wave 640^3, 7-point eta damping (N3)"] = json.dumps({
+        "damping_pass_ms_once": round(ms_eta, 4),
+        "damping_pass_frac_of_peak": round(traffic.apply_bytes(n, n, n, 1) / (ms_eta / 1e3) / 1e9 / peak, 3),
+        "step_ms": round(ms_eff, 4), "step_frac_of_peak": round(wb / (ms_eff / 1e3) / 1e9 / peak, 3)})
+    out["wave 640^3, region split, 16-point band (N1)"] = json.dumps({"ms": round(ms_pml, 4)})
+    plan.close()
+    del f, eff, nxt
+    m = 512
+    u0 = synth.uniform_field(m, m, m)
+    whole = StencilPlan(m, m, m, R, c)
+    a = torch.from_numpy(u0.ravel()).cuda()
+    b = a.clone()
+    with torch.cuda.stream(stream):
+        ms_whole = _time_loop(lambda: whole.apply(a, b, stream), 100, 10, stream)
+        whole.status(stream)
+    whole.close()
+    del a, b
+    row = {"whole_grid_ms": round(ms_whole, 4)}
+    for P in (2, 4, 8):
+        sl = StencilSlabs(m, m, m, R, c, P)
+        xs = []
+        for k in range(P):
+            e = sl.extent(k)
+            xs.append(torch.from_numpy(np.ascontiguousarray(u0[e["begin"]:e["end"]]).ravel()).cuda())
+        ys = [x.clone() for x in xs]
+        with torch.cuda.stream(stream):
+            ms = _time_loop(lambda: sl.apply(xs, ys, stream), 100, 10, stream)
+            ms_x = _time_loop(lambda: sl.exchange(xs, stream), 100, 10, stream)
+            sl.status(stream)
+        row[f"{P}_slabs_ms"] = round(ms, 4)
+        row[f"{P}_slabs_exchange_alone_ms"] = round(ms_x, 4)
+        sl.close()
+        del xs, ys
+    out["sweep 512^3 as z-slabs on one GPU (N4)"] = json.dumps(row)
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_report_configs(args):
     """Time all five workloads as their configs define them (sweeps/steps loops), plus the
     CPU oracle on a bounded sample of each; one JSON line per workload and a markdown table."""
@@ -582,6 +640,7 @@ def run_report_configs(args):
         print(json.dumps(row), flush=True)
         cmp.append(row)
         plan.close()
+    extra = run_extra_rows(torch, stream, peak)
     print("| workload | GPoints/s | HBM GB/s | % of measured peak | ms per sweep/step | B/pt DRAM (ncu) / compulsory "
           "| parity max err/tol | CPU oracle GPoints/s |")
     print("|---|---|---|---|---|---|---|---|")
@@ -591,6 +650,10 @@ def run_report_configs(args):
         print(f"| {l['workload']} | {l['gpoints_per_s']:.1f} | {l['hbm_gbs']:.0f} | {100 * l['frac_of_peak']:.1f} | "
               f"{l['ms_per_sweep_or_step']:.4f} | {dram} / {l['compulsory_bytes_per_point']:.2f} | {par} | "
               f"{l.get('cpu_oracle_gpoints_per_s', float('nan')):.2f} |")
+    print("| row | measurement |")
+    print("|---|---|")
+    for k, v in extra.items():
+        print(f"| {k} | {v} |")
     print("| sweep kernel | transposed z filter: ms, % of peak | semi-stencil: ms, % of peak |")
     print("|---|---|---|")
     for row in cmp:
