@@ -105,15 +105,17 @@ int wave_step(stencil_plan* plan, const float* u_prev, const float* u, float* u_
 
 /*
  * The same wave step for a model whose damping lives in a band of `pml_width` points
- * along the six faces ("Accelerating High-Order Stencils on GPUs" runs the inner region
- * and the PML region as separate data regions).  Precondition: eta = 0 at every point at
- * least pml_width away from all faces.  The call then skips staging eta and the divide by
- * 1+eta for every (64 x tile-height) output tile and plane that lies wholly in that
- * region, where the update is the plain leapfrog u_next = 2u - u_prev + v2dt2*lap(u), so
- * the inner region moves 16 instead of 20 bytes per point; tiles that reach into the band
- * use eta as given.  If the precondition does not hold, points outside the band are
- * computed with eta taken as 0 or as given, depending on their tile.  Same fields, layout,
- * aliasing rules and errors as wave_step; pml_width >= 0.
+ * along the six faces, run as the pages run it: one launch per data region ("Accelerating
+ * High-Order Stencils on GPUs" launches the inner region and the PML region separately).
+ * Precondition: eta = 0 at every point at least pml_width away from all faces.  The inner
+ * region (every 64 x tile-height output tile lying wholly at least pml_width from the x
+ * and y faces, over the output planes at least pml_width from the z faces) runs a kernel
+ * that stages no eta and never divides, the plain leapfrog
+ * u_next = 2u - u_prev + v2dt2*lap(u) (16 instead of 20 bytes per point); the band around
+ * it (at most six boxes, one launch) runs the full update on an internal stream beside
+ * it, and `stream` waits for both.  If the precondition does not hold, points of the inner
+ * region are computed with eta taken as 0.  Same fields, layout, aliasing rules and errors
+ * as wave_step; pml_width >= 0.
  */
 int wave_step_pml(stencil_plan* plan, const float* u_prev, const float* u, float* u_next,
                   const float* v2dt2, const float* eta, int64_t pml_width, void* stream);
@@ -124,8 +126,8 @@ int wave_step_pml(stencil_plan* plan, const float* u_prev, const float* u, float
  * use a low-order 7-point stencil, halo one; the page prints no formula).  Reading: the
  * damping at a point is the radius-1 star stencil of eta,
  *   eta_eff = e0*eta + e1*(eta at the six face neighbours),
- * at every point at least one away from every face (the faces of eta_eff get eta's
- * values).  eta does not change in time, so this runs once per model: every later
+ * written at every point at least one away from every face (the points on the faces are
+ * left as they were: no step reads them).  eta does not change in time, so this runs once per model: every later
  * wave_step / wave_step_pml / wave_steps with eta_eff in place of eta is the step with the
  * 7-point damping, at the cost of the pointwise step.  With e0 + 6*e1 = 1 a constant eta
  * is left unchanged.  eta, eta_eff: device, nx*ny*nz floats, 16-byte aligned, must not
@@ -188,7 +190,8 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
 
 /*
  * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step,
- * 2 = wave_step_pml, 3 = stencil_apply_semi), written
+ * 2 = the no-eta kernel of wave_step_pml's inner region, over the whole grid,
+ * 3 = stencil_apply_semi), written
  * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
  * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
  * Returns the number of values written, or a negative error code.
@@ -264,7 +267,8 @@ int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int radius, const 
  * The path shards this way along z, one ghost exchange of R planes each way per cut and
  * per sweep or step.  Here every slab lives on the device current at creation; the calls
  * copy ghost planes between slab arrays with device-to-device copies on an internal
- * stream, overlapped with the output planes that read no ghost plane.
+ * stream, which then also computes the output planes next to the cuts, while `stream`
+ * computes the planes that read no ghost plane; `stream` waits for both.
  *
  * stencil_slabs_create:   plans for every slab (coeffs and radius as stencil_plan_create);
  *                         NULL on failure (stencil_last_error says why).

@@ -24,22 +24,22 @@ struct KernelDesc {
 };
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
+          bool NOETA = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
                         const CUtensorMap& out, const StarParams& p) {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
-  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>
+  star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, NOETA, SEMI, DRIFT, TSTORE>
       <<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, out, p);
   return cudaGetLastError();
 }
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool PML = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
+          bool NOETA = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
 KernelDesc make_desc() {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
   return KernelDesc{
-      (const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>,
+      (const void*)star_sweep_kernel<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, NOETA, SEMI, DRIFT, TSTORE>,
       C::kThreads,
       C::kSmemBytes,
       C::TY,
@@ -47,14 +47,15 @@ KernelDesc make_desc() {
       C::BW,
       C::BH,
       TSTORE,
-      &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, PML, SEMI, DRIFT, TSTORE>};
+      &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, NOETA, SEMI, DRIFT, TSTORE>};
 }
 
-// Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `pml`: the wave step
-// that reads eta only in a band along the faces (wave_step_pml).  `semi`: the sweep with
+// Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `noeta`: the wave step
+// of a region where eta is zero (no eta staged, no divide; the inner region of
+// wave_step_pml).  `semi`: the sweep with
 // the z stencil split into halves (stencil_apply_semi).
 KernelDesc apply_kernel_desc(int radius);
 KernelDesc semi_kernel_desc(int radius);
-KernelDesc wave_kernel_desc(int radius, bool pml);
+KernelDesc wave_kernel_desc(int radius, bool noeta);
 
 }  // namespace libstencil

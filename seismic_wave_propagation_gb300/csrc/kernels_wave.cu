@@ -7,8 +7,8 @@
 
 namespace libstencil {
 
-KernelDesc wave_kernel_desc(int radius, bool pml) {
-  if (pml) {
+KernelDesc wave_kernel_desc(int radius, bool noeta) {
+  if (noeta) {
     switch (radius) {
       case 1: return make_desc<1, 1, 16, 5, 3, true, 2, 1, true>();
       case 2: return make_desc<2, 1, 16, 6, 3, true, 2, 1, true>();

@@ -88,6 +88,14 @@ struct stencil_plan {
   bool pipe_ready;
   int pipe_slabs;        // slabs of the last pipelined call (0: none yet)
   stencil_plan* eta_plan;  // radius-1 plan of the same grid for wave_eta_stencil (on first use)
+  // The band launch of wave_step_pml runs on `side`, beside the inner region's launch.
+  cudaStream_t side;
+  cudaEvent_t side_fork, side_join;
+  // Geometry of the last band width (wave_step_pml): inner region and band launches.
+  int64_t reg_pml;         // -1: none yet
+  int reg_kind;            // 2: inner and band; 1: no inner region (one full launch)
+  StarParams reg_inner, reg_band;
+  int reg_inner_grid, reg_band_grid;
 };
 
 namespace {
@@ -115,16 +123,17 @@ struct Schedule {
 
 constexpr int64_t kMaxRounds = 1 << 14;
 
-Schedule schedule(int64_t nx, int64_t ny, int R, int tile_y, int kind, int num_sms, int occupancy,
-                  int nzi, bool interior_tiles) {
-  Schedule sc{};
-  // Tiles cover x from 0 (masked stores), or from the interior origin R (TMA stores).
+// Tiles along x and y: they cover x from 0 (masked stores) or from the interior origin R
+// (TMA stores), and y from R.
+void tile_grid(int64_t nx, int64_t ny, int R, int tile_y, bool interior_tiles, int& ntx, int& nty) {
   const int64_t xext = interior_tiles ? nx - 2 * R : nx;
-  sc.ntx = (int)((xext + kTX - 1) / kTX);
-  const int nty = (int)((ny - 2 * R + tile_y - 1) / tile_y);
-  sc.ntiles = sc.ntx * nty;
+  ntx = (int)((xext + kTX - 1) / kTX);
+  nty = (int)((ny - 2 * R + tile_y - 1) / tile_y);
+}
+
+// Chunks per tile column for `ntiles` tiles and `nzi` output planes (the scan above).
+int64_t choose_chunks(int64_t ntiles, int nzi, int R, int kind, int num_sms, int occupancy) {
   const int64_t slots = (int64_t)num_sms * std::max(1, occupancy);
-  const int64_t ntiles = sc.ntiles;
   // Cost of n chunks: rounds of the round-robin schedule x steps per item; and the share
   // of the GPU's CTA slots the schedule keeps busy (a partly filled round idles the rest).
   auto plan_n = [&](int64_t n, double& cost, double& busy) {
@@ -169,10 +178,62 @@ Schedule schedule(int64_t nx, int64_t ny, int R, int tile_y, int kind, int num_s
     // refilled planes (measured at 512^3, R = 1: 2 chunks 5.7 TB/s, 7 chunks 4.9 TB/s).
     best_n = std::min<int64_t>(nzi, ((int64_t)num_sms + ntiles - 1) / ntiles);
   }
-  sc.nchunks = (int)best_n;
-  sc.nitems = (int)(ntiles * best_n);
+  return best_n;
+}
+
+Schedule schedule(int64_t nx, int64_t ny, int R, int tile_y, int kind, int num_sms, int occupancy,
+                  int nzi, bool interior_tiles) {
+  Schedule sc{};
+  int nty;
+  tile_grid(nx, ny, R, tile_y, interior_tiles, sc.ntx, nty);
+  sc.ntiles = sc.ntx * nty;
+  const int64_t slots = (int64_t)num_sms * std::max(1, occupancy);
+  sc.nchunks = (int)choose_chunks(sc.ntiles, nzi, R, kind, num_sms, occupancy);
+  sc.nitems = (int)((int64_t)sc.ntiles * sc.nchunks);
   sc.grid = (int)std::min<int64_t>(sc.nitems, slots);
   return sc;
+}
+
+// A rectangle of tiles [tx0, tx0 + ntx) x [ty0, ty0 + nty) and the output planes
+// [z0, z0 + nzi).
+struct Region {
+  int tx0, ty0, ntx, nty, z0, nzi;
+};
+
+// Several regions in one launch on `slots` CTAs: every box is cut into chunks of about T
+// output planes (thin boxes stay whole), the boxes with the longest items first, and T is
+// the one whose round-robin deal gives the smallest busiest CTA (a filling step counted as
+// 0.35 of a computing one).  Returns that busiest CTA's load in steps.
+double plan_regions(Region* rg, int nr, int R, int64_t slots, Box* box, int& nitems) {
+  std::stable_sort(rg, rg + nr, [](const Region& a, const Region& b) { return a.nzi > b.nzi; });
+  int zmax = 1;
+  for (int b = 0; b < nr; ++b) zmax = std::max(zmax, rg[b].nzi);
+  std::vector<double> load((size_t)std::max<int64_t>(1, slots));
+  double best = 1e300;
+  int best_t = zmax;
+  for (int n = 1; n <= std::min(zmax, 64); ++n) {
+    const int T = (zmax + n - 1) / n;
+    std::fill(load.begin(), load.end(), 0.0);
+    int64_t item = 0;
+    for (int b = 0; b < nr; ++b) {
+      const int c = std::min(rg[b].nzi, std::max(1, (rg[b].nzi + T / 2) / T));
+      const double len = (double)((rg[b].nzi + c - 1) / c) + 0.35 * 2 * R;
+      const int64_t cnt = (int64_t)rg[b].ntx * rg[b].nty * c;
+      for (int64_t i = 0; i < cnt; ++i, ++item) load[(size_t)(item % slots)] += len;
+    }
+    const double worst = *std::max_element(load.begin(), load.end());
+    if (worst < best * 0.999) {
+      best = worst;
+      best_t = T;
+    }
+  }
+  nitems = 0;
+  for (int b = 0; b < nr; ++b) {
+    const int c = std::min(rg[b].nzi, std::max(1, (rg[b].nzi + best_t / 2) / best_t));
+    box[b] = Box{rg[b].tx0, rg[b].ty0, rg[b].ntx, rg[b].ntx * rg[b].nty, rg[b].z0, rg[b].nzi, c, nitems};
+    nitems += box[b].ntiles * c;
+  }
+  return best;
 }
 
 // Launch geometry for the output planes [R + zoff, R + zoff + nzi) of the grid.
@@ -192,13 +253,28 @@ void geometry(const stencil_plan* p, int kind, int zoff, int nzi, StarParams& sp
   }
   const Schedule sc =
       schedule(p->nx, p->ny, R, kd.tile_y, kind, p->num_sms, p->occupancy[kind], nzi, kd.tstore);
-  sp.ntx = sc.ntx;
-  sp.ntiles = sc.ntiles;
-  sp.nzi = nzi;
-  sp.zoff = zoff;
-  sp.nchunks = sc.nchunks;
+  sp.nboxes = 1;
+  sp.box[0] = Box{0, 0, sc.ntx, sc.ntiles, R + zoff, nzi, sc.nchunks, 0};
   sp.nitems = sc.nitems;
   grid = sc.grid;
+}
+
+// Launch geometry for a list of regions (at most kMaxBoxes, none empty) on `slots` CTAs.
+// One region is chunked by the scan over round counts, several by plan_regions.
+void geometry_regions(const stencil_plan* p, int kind, Region* rg, int nr, int64_t slots,
+                      StarParams& sp, int& grid) {
+  geometry(p, kind, 0, 0, sp, grid);  // fields, coefficients, status; no work yet
+  if (nr == 1) {
+    const int ntiles = rg[0].ntx * rg[0].nty;
+    const int n = (int)choose_chunks(ntiles, rg[0].nzi, p->radius, kind, (int)slots, 1);
+    sp.nboxes = 1;
+    sp.box[0] = Box{rg[0].tx0, rg[0].ty0, rg[0].ntx, ntiles, rg[0].z0, rg[0].nzi, n, 0};
+    sp.nitems = ntiles * n;
+  } else {
+    sp.nboxes = nr;
+    plan_regions(rg, nr, p->radius, slots, sp.box, sp.nitems);
+  }
+  grid = (int)std::min<int64_t>(sp.nitems, slots);
 }
 
 void plan_geometry(stencil_plan* p, int kind) {
@@ -279,14 +355,15 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   return STENCIL_OK;
 }
 
-// Launch one sweep (kind 0, 3) or wave step (1, 2).  nzi >= 0 restricts it to the output
-// planes [R + zoff, R + zoff + nzi).
+// Launch one sweep (kind 0, 3) or wave step (1; 2 = without eta).  nzi >= 0 restricts it
+// to the output planes [R + zoff, R + zoff + nzi); `geo` (with `geo_grid` CTAs) gives the
+// work of the launch explicitly.
 int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
-           const float* eta, float* out, cudaStream_t stream, int pml = 1 << 30, int zoff = 0,
-           int nzi = -1) {
-  StarParams sp = p->params[kind];
-  int grid = p->grid[kind];
-  if (nzi >= 0) geometry(p, kind, zoff, nzi, sp, grid);
+           const float* eta, float* out, cudaStream_t stream, int zoff = 0, int nzi = -1,
+           const StarParams* geo = nullptr, int geo_grid = 0) {
+  StarParams sp = geo ? *geo : p->params[kind];
+  int grid = geo ? geo_grid : p->grid[kind];
+  if (!geo && nzi >= 0) geometry(p, kind, zoff, nzi, sp, grid);
   if (grid == 0) return STENCIL_OK;  // empty interior: nothing to do
   const KernelDesc& kd = p->kd[kind];
   const CUtensorMap *mu, *mp = nullptr, *mv = nullptr, *me = nullptr;
@@ -302,7 +379,6 @@ int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const 
   const CUtensorMap* mo = mu;
   if (kd.tstore && (rc = get_map(p, out, kTX, kd.tile_y, &mo, 1))) return rc;
   sp.out = out;
-  sp.pml = pml;
   sp.debug_skip = p->debug_mode == 1 ? 0 : -1;  // every CTA has a load 0
   // Copy the descriptors: the cache may evict entries while the launch is pending.
   const CUtensorMap a = *mu, b = *mp, c = *mv, d = *me, o = *mo;
@@ -409,7 +485,7 @@ int apply_host_pipelined(stencil_plan* p, const float* in_host, float* out_host,
     if (e == cudaSuccess) e = cudaStreamWaitEvent(comp, landed, 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(b + o0, a + o0, (o1 - o0) * 4, cudaMemcpyDeviceToDevice, comp);
     if (e != cudaSuccess) return cuda_fail(e, "pipelined copy in");
-    const int rc = launch(p, 0, a, nullptr, nullptr, nullptr, b, comp, 1 << 30, zk(k) - R, zk(k + 1) - zk(k));
+    const int rc = launch(p, 0, a, nullptr, nullptr, nullptr, b, comp, zk(k) - R, zk(k + 1) - zk(k));
     if (rc) return rc;
     e = cudaEventRecord(swept, comp);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hout, swept, 0);
@@ -421,6 +497,74 @@ int apply_host_pipelined(stencil_plan* p, const float* in_host, float* out_host,
   if (e != cudaSuccess) return cuda_fail(e, "pipeline end");
   p->pipe_slabs = K;
   return stencil_plan_status(p, user);
+}
+
+// wave_step_pml as two launches: the inner region, where eta is zero, with the kernel that
+// stages no eta and never divides; and the band along the faces (at most six boxes) with
+// the full update, launched after it on the side stream, so that the band's items take
+// the SMs the inner launch frees.  The inner region is every tile lying wholly at least
+// `pml` points from the x and y faces, over the output planes at least `pml` from the z
+// faces.  The geometry of both is kept for the last band width.
+void plan_regions_for(stencil_plan* p, int64_t pml) {
+  const int R = p->radius;
+  p->reg_pml = pml;
+  p->reg_kind = 1;
+  if (interior_empty(p)) return;
+  const KernelDesc& kd = p->kd[1];
+  const int xo = kd.tstore ? R : 0;
+  int ntx, nty;
+  tile_grid(p->nx, p->ny, R, kd.tile_y, kd.tstore, ntx, nty);
+  const int64_t TY = kd.tile_y;
+  const int bx0 = (int)std::max<int64_t>(0, (pml - xo + kTX - 1) / kTX);
+  const int bx1 = (int)std::min<int64_t>(ntx, p->nx - pml - xo >= 0 ? (p->nx - pml - xo) / kTX : 0);
+  const int by0 = (int)std::max<int64_t>(0, (pml - R + TY - 1) / TY);
+  const int by1 = (int)std::min<int64_t>(nty, p->ny - pml - R >= 0 ? (p->ny - pml - R) / TY : 0);
+  const int z0 = (int)std::max<int64_t>(R, pml), z1 = (int)std::min<int64_t>(p->nz - R, p->nz - pml);
+  if (bx0 >= bx1 || by0 >= by1 || z0 >= z1) return;  // no inner region: the full update everywhere
+  Region band[kMaxBoxes];
+  int nb = 0;
+  const int zall0 = R, zall1 = (int)p->nz - R;
+  if (z0 > zall0) band[nb++] = Region{0, 0, ntx, nty, zall0, z0 - zall0};
+  if (z1 < zall1) band[nb++] = Region{0, 0, ntx, nty, z1, zall1 - z1};
+  if (by0 > 0) band[nb++] = Region{0, 0, ntx, by0, z0, z1 - z0};
+  if (by1 < nty) band[nb++] = Region{0, by1, ntx, nty - by1, z0, z1 - z0};
+  if (bx0 > 0) band[nb++] = Region{0, by0, bx0, by1 - by0, z0, z1 - z0};
+  if (bx1 < ntx) band[nb++] = Region{bx1, by0, ntx - bx1, by1 - by0, z0, z1 - z0};
+  Region inner{bx0, by0, bx1 - bx0, by1 - by0, z0, z1 - z0};
+  // Both launches are planned on all CTA slots and run side by side; the band's items
+  // take the slots the inner launch leaves or frees.  (Dividing the slots between them in
+  // proportion to their work, or running the band after the inner region, measured slower.)
+  // Split only where the inner region holds at least 3/4 of the work: its points cost 0.93
+  // of the band's (640^3: 0.744 ms for a step with no eta anywhere, 0.80 ms with eta), and
+  // a thicker band of 64-wide tiles costs more in packing than that saves (640^3, 16-point
+  // band: inner share 0.71, split 1.6 % slower; 1024^3: 0.83, 13 % faster).
+  const double all = (double)ntx * nty * (zall1 - zall0);
+  if ((double)inner.ntx * inner.nty * inner.nzi < 0.75 * all) return;
+  const int64_t slots = (int64_t)p->num_sms * std::max(1, std::min(p->occupancy[1], p->occupancy[2]));
+  geometry_regions(p, 2, &inner, 1, slots, p->reg_inner, p->reg_inner_grid);
+  p->reg_band_grid = 0;
+  if (nb > 0) geometry_regions(p, 1, band, nb, slots, p->reg_band, p->reg_band_grid);
+  p->reg_kind = 2;
+}
+
+int wave_step_regions(stencil_plan* p, const float* u_prev, const float* u, float* u_next,
+                      const float* v2dt2, const float* eta, int64_t pml, cudaStream_t s) {
+  if (p->reg_pml != pml) plan_regions_for(p, pml);
+  if (p->reg_kind == 1) return launch(p, 1, u, u_prev, v2dt2, eta, u_next, s);
+  const bool band = p->reg_band_grid > 0;
+  cudaError_t e = cudaSuccess;
+  if (band) {  // the band may start once the work before this step is done, not the inner part
+    e = cudaEventRecord(p->side_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->side_fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "band fork");
+  }
+  int rc = launch(p, 2, u, u_prev, v2dt2, eta, u_next, s, 0, -1, &p->reg_inner, p->reg_inner_grid);
+  if (rc || !band) return rc;
+  if ((rc = launch(p, 1, u, u_prev, v2dt2, eta, u_next, p->side, 0, -1, &p->reg_band, p->reg_band_grid)))
+    return rc;
+  e = cudaEventRecord(p->side_join, p->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p->side_join, 0);
+  return e == cudaSuccess ? STENCIL_OK : cuda_fail(e, "band join");
 }
 
 }  // namespace
@@ -453,6 +597,7 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
     return nullptr;
   }
   stencil_plan* p = new stencil_plan();
+  p->reg_pml = -1;
   p->nx = nx;
   p->ny = ny;
   p->nz = nz;
@@ -462,6 +607,10 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e == cudaSuccess) e = cudaMalloc(&p->d_status, 4 * sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, 4 * sizeof(unsigned));
+  // The side stream of wave_step_pml's band launch (created here, not under a capture).
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->side_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->side_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cuda_fail(e, "plan setup");
     stencil_plan_destroy(p);
@@ -489,6 +638,9 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
 
 void stencil_plan_destroy(stencil_plan* p) {
   if (!p) return;
+  if (p->side) cudaStreamDestroy(p->side);
+  if (p->side_fork) cudaEventDestroy(p->side_fork);
+  if (p->side_join) cudaEventDestroy(p->side_join);
   if (p->eta_plan) stencil_plan_destroy(p->eta_plan);
   if (p->graph) cudaGraphExecDestroy(p->graph);
   if (p->pipe_ready) {
@@ -552,8 +704,8 @@ int wave_step_pml(stencil_plan* p, const float* u_prev, const float* u, float* u
   if (overlap(u_next, eta, bytes)) return fail(STENCIL_ERR_ALIAS, "u_next overlaps eta");
   if (u_next != u_prev && overlap(u_next, u_prev, bytes))
     return fail(STENCIL_ERR_ALIAS, "u_next partially overlaps u_prev");
-  const int pml = (int)std::min<int64_t>(pml_width, 1 << 30);
-  return launch(p, 2, u, u_prev, v2dt2, eta, u_next, static_cast<cudaStream_t>(stream), pml);
+  return wave_step_regions(p, u_prev, u, u_next, v2dt2, eta, std::min<int64_t>(pml_width, 1 << 30),
+                           static_cast<cudaStream_t>(stream));
 }
 
 int wave_eta_stencil(stencil_plan* p, const float* eta, float* eta_eff, float e0, float e1, void* stream) {
@@ -574,10 +726,7 @@ int wave_eta_stencil(stencil_plan* p, const float* eta, float* eta_eff, float e0
     q->c[1] = e1;
     for (int k = 0; k < 4; ++k) plan_geometry(q, k);
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(eta_eff, eta, bytes, cudaMemcpyDeviceToDevice, s);  // the faces
-  if (e != cudaSuccess) return cuda_fail(e, "eta copy");
-  return launch(q, 0, eta, nullptr, nullptr, nullptr, eta_eff, s);
+  return launch(q, 0, eta, nullptr, nullptr, nullptr, eta_eff, static_cast<cudaStream_t>(stream));
 }
 
 int stencil_sweeps(stencil_plan* p, float* a, float* b, int nsweeps, int use_graph, void* stream) {
@@ -619,18 +768,18 @@ int wave_steps(stencil_plan* p, float* u_prev, float* u, float* u_tmp, const flo
     if (overlap(bufs[i], v2dt2, bytes) || overlap(bufs[i], eta, bytes))
       return fail(STENCIL_ERR_ALIAS, "a time level overlaps v2dt2 or eta");
   }
-  const int kind = pml_width >= 0 ? 2 : 1;
-  const int pml = pml_width >= 0 ? (int)std::min<int64_t>(pml_width, 1 << 30) : (1 << 30);
+  const int64_t pml = pml_width >= 0 ? std::min<int64_t>(pml_width, 1 << 30) : -1;
   const uint64_t key[8] = {2, (uint64_t)(uintptr_t)u_prev, (uint64_t)(uintptr_t)u,
                            (uint64_t)(uintptr_t)u_tmp, (uint64_t)(uintptr_t)v2dt2,
-                           (uint64_t)(uintptr_t)eta, ((uint64_t)nsteps << 32) | (uint32_t)pml,
+                           (uint64_t)(uintptr_t)eta, ((uint64_t)nsteps << 32) | (uint32_t)(pml + 1),
                            (uint64_t)p->debug_mode};
   return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
     float* x = u_prev;
     float* y = u;
     float* z = u_tmp;
     for (int i = 0; i < nsteps; ++i) {
-      const int r = launch(p, kind, y, x, v2dt2, eta, z, s, pml);
+      const int r = pml >= 0 ? wave_step_regions(p, x, y, z, v2dt2, eta, pml, s)
+                             : launch(p, 1, y, x, v2dt2, eta, z, s);
       if (r) return r;
       float* t = x;  // rotate: (prev, cur, next) <- (cur, next, prev)
       x = y;
@@ -721,8 +870,8 @@ int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int
   if (!p || !info || n < 0 || kind < 0 || kind > 3) return fail(STENCIL_ERR_ARG, "bad arguments");
   const KernelDesc& kd = p->kd[kind];
   const StarParams& sp = p->params[kind];
-  const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.ntiles,
-                         sp.nchunks,    kTX,        kd.tile_y, kd.stages,       p->num_sms};
+  const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.box[0].ntiles,
+                         sp.box[0].nchunks, kTX,    kd.tile_y, kd.stages,       p->num_sms};
   const int m = std::min(n, 10);
   for (int i = 0; i < m; ++i) info[i] = v[i];
   return m;
@@ -951,7 +1100,7 @@ int slab_run(stencil_slabs* S, int kind, float* const* x, float* const* uprev, f
     if (hi <= lo) return (int)STENCIL_OK;
     stencil_plan* p = S->plans[k];
     return launch(p, kind, x[k], uprev ? uprev[k] : nullptr, v2dt2 ? v2dt2[k] : nullptr,
-                  eta ? eta[k] : nullptr, out[k], st, 1 << 30, (int)(lo - R), (int)(hi - lo));
+                  eta ? eta[k] : nullptr, out[k], st, (int)(lo - R), (int)(hi - lo));
   };
   if (P > 1) {
     cudaError_t e = cudaEventRecord(S->fork, s);
@@ -962,23 +1111,28 @@ int slab_run(stencil_slabs* S, int kind, float* const* x, float* const* uprev, f
     const int rc = run(k, in_lo[k], in_hi[k], s);
     if (rc) return rc;
   }
+  // The planes next to the cuts follow the copies on the exchange stream, so they run
+  // alongside the interior launches instead of after them.
+  cudaStream_t bs = P > 1 ? S->copy : s;
   if (P > 1) {
-    int rc = slab_exchange(S, x, S->copy);
+    const int rc = slab_exchange(S, x, bs);
     if (rc) return rc;
-    cudaError_t e = cudaEventRecord(S->join, S->copy);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, S->join, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "exchange join");
   }
   for (int k = 0; k < P; ++k) {
     const int64_t nzk = slab_end(S, k) - slab_begin(S, k);
     int rc;
     if (in_hi[k] <= in_lo[k]) {
-      rc = run(k, R, nzk - R, s);
+      rc = run(k, R, nzk - R, bs);
     } else {
-      rc = run(k, R, in_lo[k], s);
-      if (!rc) rc = run(k, in_hi[k], nzk - R, s);
+      rc = run(k, R, in_lo[k], bs);
+      if (!rc) rc = run(k, in_hi[k], nzk - R, bs);
     }
     if (rc) return rc;
+  }
+  if (P > 1) {
+    cudaError_t e = cudaEventRecord(S->join, bs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, S->join, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "exchange join");
   }
   return STENCIL_OK;
 }

@@ -51,19 +51,29 @@ constexpr unsigned kStatusDrainTimeout = 2u;
 constexpr unsigned kStatusBadSmem = 4u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// A box of work: a rectangle of output tiles times a range of output planes, cut into
+// z-chunks; every (tile, chunk) pair is one work item.
+struct Box {
+  int tx0, ty0;     // first tile along x and y
+  int ntx;          // tiles along x
+  int ntiles;       // tiles in the rectangle
+  int z0;           // first output plane
+  int nzi;          // output planes
+  int nchunks;      // z-chunks per tile column
+  int item0;        // index of the box's first work item
+};
+
+constexpr int kMaxBoxes = 6;
+
 struct StarParams {
   int nx, ny, nz;
-  int ntx;          // tiles along x
-  int ntiles;       // tiles per plane
-  int nzi;          // output planes of this launch (nz - 2R for the whole grid)
-  int zoff;         // first output plane of this launch minus R (0 for the whole grid)
-  int nchunks;      // z chunks per tile column
-  int nitems;       // ntiles * nchunks
+  int nboxes;       // boxes of this launch (one for a whole-grid sweep or step)
+  int nitems;       // work items of all boxes
+  Box box[kMaxBoxes];
   float c[5];       // c[0] total centre weight, c[r] per-neighbour weight
   float* out;       // stencil output, or u_next for the wave step
   unsigned* status; // [0] flags, [1] block, [2] load counter of the first failure
   int debug_skip;   // load counter every CTA skips (watchdog test); -1 = none
-  int pml;          // wave step with a face band: eta is zero beyond `pml` points from the faces
 };
 
 // Producer cursor: the next load of the CTA's sequence (kept in shared memory; the warps
@@ -236,25 +246,21 @@ __device__ __forceinline__ float get(const float4& v, int e) {
 template <int R, int TY, int XO>
 __device__ __forceinline__ void item_geometry(const StarParams& p, int item, int& x0, int& y0,
                                               int& L, int& zs, int& dz) {
-  const int chunk = item / p.ntiles;
-  const int tile = item - chunk * p.ntiles;
-  const int by = tile / p.ntx;
-  const int bx = tile - by * p.ntx;
-  x0 = XO + bx * kTX;
-  y0 = R + by * TY;
-  const int za = R + p.zoff + (int)(((long long)chunk * p.nzi) / p.nchunks);
-  const int zb = R + p.zoff + (int)(((long long)(chunk + 1) * p.nzi) / p.nchunks);
+  int b = 0;
+  while (b + 1 < p.nboxes && item >= p.box[b + 1].item0) ++b;
+  const Box& q = p.box[b];
+  const int local = item - q.item0;
+  const int chunk = local / q.ntiles;
+  const int tile = local - chunk * q.ntiles;
+  const int by = tile / q.ntx;
+  const int bx = tile - by * q.ntx;
+  x0 = XO + (q.tx0 + bx) * kTX;
+  y0 = R + (q.ty0 + by) * TY;
+  const int za = q.z0 + (int)(((long long)chunk * q.nzi) / q.nchunks);
+  const int zb = q.z0 + (int)(((long long)(chunk + 1) * q.nzi) / q.nchunks);
   L = zb - za + 2 * R;
   dz = 1;
   zs = za - R;
-}
-
-// Does the wave step need eta for the output tile at (x0, y0), plane z?  Only where the
-// tile reaches into the band of `pml` points along the faces; elsewhere eta is zero.
-template <int TY>
-__device__ __forceinline__ bool tile_needs_eta(const StarParams& p, int x0, int y0, int z) {
-  return z < p.pml || z >= p.nz - p.pml || x0 < p.pml || x0 + kTX > p.nx - p.pml || y0 < p.pml ||
-         y0 + TY > p.ny - p.pml;
 }
 
 template <int R, int TY, int XO>
@@ -271,7 +277,7 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 
 // ---- the kernel ----------------------------------------------------------------------
 
-template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool PML,
+template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool NOETA,
           bool SEMI, bool DRIFT, bool TSTORE>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
@@ -336,11 +342,10 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     if (k.j >= 2 * R) {
       const uint32_t dst = aux_base + slot * C::kAuxStageBytes;
       const int z = k.zs + k.dz * (k.j - R);
-      const bool eta = !PML || tile_needs_eta<TY>(p, k.x0, k.y0, z);
-      mbar_arrive_expect_tx(bar, (eta ? 3 : 2) * C::kAuxFieldBytes);
+      mbar_arrive_expect_tx(bar, (NOETA ? 2 : 3) * C::kAuxFieldBytes);
       tma_load_3d(dst, &tm_uprev, bar, k.x0, k.y0, z);
       tma_load_3d(dst + C::kAuxFieldBytes, &tm_v2dt2, bar, k.x0, k.y0, z);
-      if (eta) tma_load_3d(dst + 2 * C::kAuxFieldBytes, &tm_eta, bar, k.x0, k.y0, z);
+      if (!NOETA) tma_load_3d(dst + 2 * C::kAuxFieldBytes, &tm_eta, bar, k.x0, k.y0, z);
     } else {
       mbar_arrive(bar);  // filling step: nothing to stage, just complete the phase
     }
@@ -429,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
           int cs = slot - R;
           if (cs < 0) cs += STAGES;
           const float* pu = ring + cs * PSTRIDE + own;  // u at plane z (landed R steps ago)
-          if (!PML || tile_needs_eta<TY>(p, x0, y0, z)) {
+          if constexpr (!NOETA) {
 #pragma unroll
             for (int k = 0; k < TYT; ++k) {
               const int a = (row0 + k) * kTX + col;
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
                 pset(o[k], e, __fdividef(t, 1.0f + eta));  // 1 + eta in [1, 2]: 2-ulp divide
               }
             }
-          } else {  // the tile lies where eta = 0: plain leapfrog, no eta staged, no divide
+          } else {  // a region where eta = 0: plain leapfrog, no eta staged, no divide
 #pragma unroll
             for (int k = 0; k < TYT; ++k) {
               const int a = (row0 + k) * kTX + col;
