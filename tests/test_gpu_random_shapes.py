@@ -73,3 +73,53 @@ def test_random_shape_wave_step(nx, ny, nz, R):
         tol = 1e-5 * (2 + 0.2 * float(np.sum(np.abs(c)))) * 2.0
         assert np.max(np.abs(got[m] - want[m])) <= tol
     assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD)
+
+
+def split_shapes(seed: int, count: int):
+    """Shapes (all radii) on which wave_step_pml runs as two launches: the inner region
+    holds at least 3/4 of the tiles x planes (64-wide tiles from x = 0, 16-high tiles from
+    y = R).  Band widths are drawn from 0-6, but at these sizes only width 0 passes, so
+    these cases run the no-eta kernel on ragged grids beside a thin band launch; wider
+    bands are covered on larger grids in the wave tests."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(100 * count):
+        if len(out) == count:
+            break
+        R = int(rng.integers(1, 5))
+        nx, ny, nz = 64 * int(rng.integers(2, 7)), int(rng.integers(60, 200)), int(rng.integers(20, 70))
+        pml = int(rng.integers(0, 7))
+        ntx, nty = -(-nx // 64), -(-(ny - 2 * R) // 16)
+        bx = max(0, min(ntx, (nx - pml) // 64) - (-(-pml // 64)))
+        by = max(0, min(nty, (ny - pml - R) // 16) - max(0, -(-(pml - R) // 16)))
+        bz = max(0, min(nz - R, nz - pml) - max(R, pml))
+        if bx * by * bz >= 0.75 * ntx * nty * (nz - 2 * R):
+            out.append((nx, ny, nz, R, pml))
+    return out
+
+
+@pytest.mark.parametrize("nx,ny,nz,R,pml", split_shapes(2026, 10))
+def test_random_shape_region_split_step(nx, ny, nz, R, pml):
+    torch = torch_cuda()
+    seed = nx + 3 * ny + 5 * nz + R + 7 * pml
+    up = synth.uniform_field(nx, ny, nz, seed=seed)
+    u = synth.uniform_field(nx, ny, nz, seed=seed + 1)
+    s = synth.uniform_field(nx, ny, nz, seed=seed + 2, scale=0.1) + np.float32(0.1)
+    z, y, x = np.meshgrid(*[np.arange(n) for n in (nz, ny, nx)], indexing="ij")
+    d = np.minimum.reduce([x, nx - 1 - x, y, ny - 1 - y, z, nz - 1 - z])
+    e = np.where(d < pml, synth.uniform_field(nx, ny, nz, seed=seed + 3, scale=0.05) + np.float32(0.05),
+                 np.float32(0.0)).astype(np.float32)
+    c = np.random.default_rng(seed).uniform(-0.3, 0.3, R + 1)
+    plan = StencilPlan(nx, ny, nz, R, c)
+    gs = [Guarded(torch, a) for a in (up, u, s, e)]
+    gn = Guarded(torch, u, fill_sentinel=True)
+    plan.wave_step_pml(gs[0].ptr, gs[1].ptr, gn.ptr, gs[2].ptr, gs[3].ptr, pml)
+    plan.status()
+    got = gn.numpy()
+    assert all(g.guards_intact() for g in gs + [gn])
+    plan.close()
+    want = oracle.wave_step(up, u, s, e, np.asarray(c, np.float32), R, u_next=np.zeros_like(u))
+    m = interior_mask(u.shape, R)
+    tol = 1e-5 * (2 + 0.2 * float(np.sum(np.abs(c)))) * 2.0
+    assert np.max(np.abs(got[m] - want[m])) <= tol
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD)
