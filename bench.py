@@ -425,22 +425,27 @@ def run_profile_case(kind: str):
     import torch
     from seismic_wave_propagation_gb300 import StencilPlan
     n = NX
-    r = 1 if kind == "sweep7" else R
-    c = synth.laplacian2_coeffs() if kind == "sweep7" else synth.laplacian8_coeffs()
+    r = 1 if kind in ("sweep7", "sweep7x2") else R
+    c = synth.laplacian2_coeffs() if r == 1 else synth.laplacian8_coeffs()
     plan = StencilPlan(n, n, n, r, c)
-    if kind in ("sweep", "semi", "sweep7"):
+    if kind in ("sweep", "semi", "sweep7", "sweep7x2"):
         u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
         o = u.clone()
+        fn = {"semi": plan.apply_semi, "sweep7x2": plan.apply2}.get(kind, plan.apply)
         for _ in range(3):
-            (plan.apply_semi if kind == "semi" else plan.apply)(u, o)
+            fn(u, o)
     else:
         f = [torch.from_numpy(a.ravel()).cuda() for a in synth.wave_fields(n, n, n)]
         nxt = f[0].clone()
         for _ in range(3):
-            plan.wave_step(f[0], f[1], nxt, f[2], f[3])
+            if kind == "wave_inner":  # no band: the inner region's kernel covers all but one tile row
+                plan.wave_step_pml(f[0], f[1], nxt, f[2], f[3], 0)
+            else:
+                plan.wave_step(f[0], f[1], nxt, f[2], f[3])
     torch.cuda.synchronize()
     plan.status()
-    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info({"sweep": 0, "sweep7": 0, "wave": 1, "semi": 3}[kind])}))
+    k = {"sweep": 0, "sweep7": 0, "wave": 1, "wave_inner": 2, "semi": 3, "sweep7x2": 4}[kind]
+    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info(k)}))
 
 
 def _time_loop(fn, steps, warmup, stream, warm_seconds=0.3):
@@ -670,8 +675,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
-    ap.add_argument("--profile", choices=["sweep", "sweep7", "wave", "semi"],
-                    help="run 3 launches of the 512^3 case (ncu driver); sweep7 is the 7-point Laplacian")
+    ap.add_argument("--profile", choices=["sweep", "sweep7", "sweep7x2", "wave", "wave_inner", "semi"],
+                    help="run 3 launches of the 512^3 case (ncu driver); sweep7 is the 7-point Laplacian, "
+                         "sweep7x2 its two-sweep pass, wave_inner the band step with no band (no-eta kernel)")
     ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
     if args.profile or args.report_configs:

@@ -75,6 +75,18 @@ void stencil_plan_destroy(stencil_plan* plan);
 int stencil_apply(stencil_plan* plan, const float* in, float* out, void* stream);
 
 /*
+ * Two sweeps in one pass: out = S(S(in)) for the plan's stencil S (temporal blocking of
+ * the ping-pong loop), with the shell of every level held at in's values, i.e. exactly
+ * what two stencil_apply calls in -> tmp -> out compute when out and tmp start with in's
+ * shell.  The intermediate level stays in shared memory, so the pass reads and writes the
+ * grid once for two sweeps.  Built for radius 1 (the 7-point stencil); other radii return
+ * STENCIL_ERR_ARG.  Same arguments, layout, aliasing rules and errors as stencil_apply;
+ * the shell of `out` is untouched.  stencil_sweeps and stencil_apply_host use it for most
+ * of a radius-1 loop.
+ */
+int stencil_apply2(stencil_plan* plan, const float* in, float* out, void* stream);
+
+/*
  * The same sweep computed in semi-stencil form ("Accelerating High-Order Stencils on
  * GPUs", the semi-stencil strategy: a stencil along one axis is split into a forward and
  * a backward half, so the centre and one half are read together and the other half is
@@ -142,7 +154,8 @@ int wave_eta_stencil(stencil_plan* plan, const float* eta, float* eta_eff, float
  * stream, as the benchmark workloads run them).
  *
  * stencil_sweeps: `nsweeps` ping-pong sweeps a -> b -> a -> ...; after an even count the
- *   result is in a, after an odd count in b.  Both buffers keep their shells (start them
+ *   result is in a, after an odd count in b.  For radius 1, 2*floor(nsweeps/4) passes of
+ *   stencil_apply2 carry most of them (each pass two sweeps), the rest are single sweeps.  Both buffers keep their shells (start them
  *   as two copies of the same field for a fixed boundary).  a and b must not overlap.
  * wave_steps: `nsteps` wave steps with three-buffer rotation: each step computes the next
  *   level into the buffer of the oldest one, so after n steps the newest level is in
@@ -191,7 +204,7 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
 /*
  * Launch geometry the plan chose for `kind` (0 = stencil_apply, 1 = wave_step,
  * 2 = the no-eta kernel of wave_step_pml's inner region, over the whole grid,
- * 3 = stencil_apply_semi), written
+ * 3 = stencil_apply_semi, 4 = stencil_apply2 (radius 1 only)), written
  * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
  * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
  * Returns the number of values written, or a negative error code.

@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "libstencil.h")
 STENCIL_OK = 0
 ERRORS = {-1: "STENCIL_ERR_ARG", -2: "STENCIL_ERR_ALIGNMENT", -3: "STENCIL_ERR_ALIAS",
           -4: "STENCIL_ERR_CUDA", -5: "STENCIL_ERR_TIMEOUT"}
-KIND_APPLY, KIND_WAVE, KIND_WAVE_PML, KIND_SEMI = 0, 1, 2, 3
+KIND_APPLY, KIND_WAVE, KIND_WAVE_PML, KIND_SEMI, KIND_APPLY2 = 0, 1, 2, 3, 4
 LAUNCH_INFO_KEYS = ("grid", "threads", "smem", "ctas_per_sm", "tiles", "zchunks", "tile_x",
                     "tile_y", "stages", "sms")
 
@@ -58,6 +58,7 @@ def load():
         lib.stencil_plan_destroy.restype = None
         lib.stencil_apply.argtypes = [vp, vp, vp, vp]
         lib.stencil_apply_semi.argtypes = [vp, vp, vp, vp]
+        lib.stencil_apply2.argtypes = [vp, vp, vp, vp]
         lib.wave_step.argtypes = [vp] * 7
         lib.wave_step_pml.argtypes = [vp] * 6 + [i64, vp]
         lib.stencil_plan_status.argtypes = [vp, vp]
@@ -82,7 +83,7 @@ def load():
         lib.stencil_slabs_apply.argtypes = [vp, vp, vp, vp]
         lib.stencil_slabs_wave_step.argtypes = [vp] * 7
         lib.stencil_slabs_status.argtypes = [vp, vp]
-        for fn in ("stencil_apply", "stencil_apply_semi", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
+        for fn in ("stencil_apply", "stencil_apply_semi", "stencil_apply2", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
                    "stencil_plan_status", "stencil_apply_host",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject",
                    "stencil_schedule_query", "stencil_plan_host_phases", "wave_eta_stencil", "stencil_slabs_extent",
@@ -172,6 +173,10 @@ class StencilPlan:
 
     def apply(self, inp, out, stream=None) -> None:
         _check(self._lib.stencil_apply(self._p, _addr(inp), _addr(out), _stream(stream, inp, out)))
+
+    def apply2(self, inp, out, stream=None) -> None:
+        """stencil_apply2: two sweeps in one pass (radius 1): out = S(S(inp))."""
+        _check(self._lib.stencil_apply2(self._p, _addr(inp), _addr(out), _stream(stream, inp, out)))
 
     def apply_semi(self, inp, out, stream=None) -> None:
         """The same sweep in semi-stencil form (an alternative kernel; see the header)."""

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "star2_kernels.cuh"
 #include "star_kernels.cuh"
 
 namespace libstencil {
@@ -50,11 +51,30 @@ KernelDesc make_desc() {
       &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, NOETA, SEMI, DRIFT, TSTORE>};
 }
 
+// Two radius-1 sweeps in one pass (star2_kernels.cuh).
+template <int STAGES, int MINB>
+cudaError_t launch_star2(dim3 grid, cudaStream_t stream, const CUtensorMap& u, const CUtensorMap& uprev,
+                         const CUtensorMap& v2dt2, const CUtensorMap& eta, const CUtensorMap& out,
+                         const StarParams& p) {
+  using C = Star2Cfg<STAGES>;
+  star2_sweep_kernel<STAGES, MINB><<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, out, p);
+  return cudaGetLastError();
+}
+
+template <int STAGES, int MINB>
+KernelDesc make_desc2() {
+  using C = Star2Cfg<STAGES>;
+  return KernelDesc{(const void*)star2_sweep_kernel<STAGES, MINB>, C::kThreads, C::kSmemBytes, C::TY, STAGES,
+                    C::BW, C::BH, false, &launch_star2<STAGES, MINB>};
+}
+
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `noeta`: the wave step
 // of a region where eta is zero (no eta staged, no divide; the inner region of
 // wave_step_pml).  `semi`: the sweep with
 // the z stencil split into halves (stencil_apply_semi).
 KernelDesc apply_kernel_desc(int radius);
+// Two sweeps in one pass: built for radius 1 (fn is null for other radii).
+KernelDesc apply2_kernel_desc(int radius);
 KernelDesc semi_kernel_desc(int radius);
 KernelDesc wave_kernel_desc(int radius, bool noeta);
 

@@ -18,6 +18,13 @@ KernelDesc apply_kernel_desc(int radius) {
   }
 }
 
+// Two radius-1 sweeps per pass: 64 x 30 output tiles, 256 threads, a 5-slot ring.
+KernelDesc apply2_kernel_desc(int radius) {
+  if (radius == 1) return make_desc2<5, 2>();
+  KernelDesc none{};
+  return none;
+}
+
 // Semi-stencil sweeps: the ring also keeps the R planes behind the lead (the left half of
 // the z stencil is read from them), so it holds 2R + 1 slots or more.
 KernelDesc semi_kernel_desc(int radius) {

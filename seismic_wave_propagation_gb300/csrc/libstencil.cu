@@ -69,10 +69,12 @@ struct stencil_plan {
   float c[STENCIL_MAX_RADIUS + 1];
   int device;
   int num_sms;
-  KernelDesc kd[4];    // [0] apply, [1] wave, [2] wave with eta in a face band, [3] semi apply
-  int occupancy[4];    // CTAs per SM
-  StarParams params[4];
-  int grid[4];
+  // [0] apply, [1] wave, [2] wave without eta (inner region of wave_step_pml), [3] semi
+  // apply, [4] two sweeps in one pass (radius 1 only; fn null otherwise)
+  KernelDesc kd[5];
+  int occupancy[5];    // CTAs per SM
+  StarParams params[5];
+  int grid[5];
   unsigned* d_status;  // 4 words
   MapEntry maps[kMapCache];
   uint64_t clock;
@@ -567,6 +569,25 @@ int wave_step_regions(stencil_plan* p, const float* u_prev, const float* u, floa
   return e == cudaSuccess ? STENCIL_OK : cuda_fail(e, "band join");
 }
 
+// `n` ping-pong sweeps x -> y -> x ... on stream s.  Where the plan has the two-sweep
+// kernel (radius 1) most of them run in pairs, one pass per pair; the number of such
+// passes is kept even so that the result lands where n single sweeps would leave it
+// (x for even n, y for odd n): 2*floor(n/4) passes, then the rest one by one.
+int ping_pong(stencil_plan* p, float* x, float* y, int n, cudaStream_t s) {
+  const int pairs = p->kd[4].fn ? 2 * (n / 4) : 0;
+  for (int i = 0; i < pairs; ++i) {
+    const int r = launch(p, 4, x, nullptr, nullptr, nullptr, y, s);
+    if (r) return r;
+    std::swap(x, y);
+  }
+  for (int i = 2 * pairs; i < n; ++i) {
+    const int r = launch(p, 0, x, nullptr, nullptr, nullptr, y, s);
+    if (r) return r;
+    std::swap(x, y);
+  }
+  return STENCIL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -620,7 +641,9 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
   p->kd[1] = wave_kernel_desc(radius, false);
   p->kd[2] = wave_kernel_desc(radius, true);
   p->kd[3] = semi_kernel_desc(radius);
-  for (int k = 0; k < 4; ++k) {
+  p->kd[4] = apply2_kernel_desc(radius);
+  for (int k = 0; k < 5; ++k) {
+    if (!p->kd[k].fn) continue;  // not built for this radius
     e = cudaFuncSetAttribute(p->kd[k].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->kd[k].smem);
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p->occupancy[k], p->kd[k].fn,
@@ -659,6 +682,16 @@ int stencil_apply(stencil_plan* p, const float* in, float* out, void* stream) {
   if ((rc = check_field(p, in, "in")) || (rc = check_field(p, out, "out"))) return rc;
   if (overlap(in, out, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
   return launch(p, 0, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
+}
+
+int stencil_apply2(stencil_plan* p, const float* in, float* out, void* stream) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (!p->kd[4].fn) return fail(STENCIL_ERR_ARG, "two sweeps per pass are built for radius 1, not %d", p->radius);
+  int rc = check_device(p);
+  if (rc) return rc;
+  if ((rc = check_field(p, in, "in")) || (rc = check_field(p, out, "out"))) return rc;
+  if (overlap(in, out, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");
+  return launch(p, 4, in, nullptr, nullptr, nullptr, out, static_cast<cudaStream_t>(stream));
 }
 
 int stencil_apply_semi(stencil_plan* p, const float* in, float* out, void* stream) {
@@ -724,7 +757,8 @@ int wave_eta_stencil(stencil_plan* p, const float* eta, float* eta_eff, float e0
   if (q->c[0] != e0 || q->c[1] != e1) {  // new weights: the launch parameters carry them
     q->c[0] = e0;
     q->c[1] = e1;
-    for (int k = 0; k < 4; ++k) plan_geometry(q, k);
+    for (int k = 0; k < 5; ++k)
+      if (q->kd[k].fn) plan_geometry(q, k);
   }
   return launch(q, 0, eta, nullptr, nullptr, nullptr, eta_eff, static_cast<cudaStream_t>(stream));
 }
@@ -738,16 +772,8 @@ int stencil_sweeps(stencil_plan* p, float* a, float* b, int nsweeps, int use_gra
   if (overlap(a, b, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "a and b overlap");
   const uint64_t key[8] = {1, (uint64_t)(uintptr_t)a, (uint64_t)(uintptr_t)b, (uint64_t)nsweeps,
                            (uint64_t)p->debug_mode, 0, 0, 0};
-  return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream), [&](cudaStream_t s) {
-    float* x = a;
-    float* y = b;
-    for (int i = 0; i < nsweeps; ++i) {
-      const int r = launch(p, 0, x, nullptr, nullptr, nullptr, y, s);
-      if (r) return r;
-      std::swap(x, y);
-    }
-    return (int)STENCIL_OK;
-  });
+  return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream),
+                  [&](cudaStream_t s) { return ping_pong(p, a, b, nsweeps, s); });
 }
 
 int wave_steps(stencil_plan* p, float* u_prev, float* u, float* u_tmp, const float* v2dt2,
@@ -827,10 +853,8 @@ int stencil_apply_host(stencil_plan* p, const float* in_host, float* out_host, i
   cudaError_t e = cudaMemcpyAsync(a, in_host, n * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && nsweeps > 0) e = cudaMemcpyAsync(b, a, n * 4, cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "copy in");
-  for (int i = 0; i < nsweeps; ++i) {
-    if ((rc = launch(p, 0, a, nullptr, nullptr, nullptr, b, s))) return rc;
-    std::swap(a, b);
-  }
+  if ((rc = ping_pong(p, a, b, nsweeps, s))) return rc;
+  if (nsweeps % 2) std::swap(a, b);
   e = cudaMemcpyAsync(out_host, a, n * 4, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e, "copy out");
   return stencil_plan_status(p, stream);
@@ -867,7 +891,8 @@ int wave_run_host(stencil_plan* p, float* u_prev_host, float* u_host, const floa
 }
 
 int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int n) {
-  if (!p || !info || n < 0 || kind < 0 || kind > 3) return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (!p || !info || n < 0 || kind < 0 || kind > 4) return fail(STENCIL_ERR_ARG, "bad arguments");
+  if (!p->kd[kind].fn) return fail(STENCIL_ERR_ARG, "kind %d is not built for radius %d", kind, p->radius);
   const KernelDesc& kd = p->kd[kind];
   const StarParams& sp = p->params[kind];
   const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.box[0].ntiles,
@@ -895,7 +920,7 @@ int stencil_plan_host_phases(const stencil_plan* p, float* ms, int n) {
 
 int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int kind, int num_sms,
                            int ctas_per_sm, int64_t* info, int n) {
-  if (radius < 1 || radius > STENCIL_MAX_RADIUS || kind < 0 || kind > 3 || num_sms < 1 ||
+  if (radius < 1 || radius > STENCIL_MAX_RADIUS || kind < 0 || kind > 4 || num_sms < 1 ||
       ctas_per_sm < 1 || !info || n < 0)
     return fail(STENCIL_ERR_ARG, "bad arguments");
   if (nx < 1 || ny < 1 || nz < 1 || nx > (1 << 30) || ny > (1 << 30) || nz > (1 << 30) ||
@@ -904,7 +929,9 @@ int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int k
                 (long long)ny, (long long)nz);
   const KernelDesc kd = kind == 0   ? apply_kernel_desc(radius)
                         : kind == 3 ? semi_kernel_desc(radius)
+                        : kind == 4 ? apply2_kernel_desc(radius)
                                     : wave_kernel_desc(radius, kind == 2);
+  if (!kd.fn) return fail(STENCIL_ERR_ARG, "kind %d is not built for radius %d", kind, radius);
   const int64_t m = 2 * (int64_t)radius + 1;
   Schedule sc{};
   if (nx >= m && ny >= m && nz >= m)

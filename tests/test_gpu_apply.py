@@ -323,3 +323,64 @@ def test_two_plans_on_two_streams_concurrently():
         p.status(s)
         assert torch.equal(b, ref)
         p.close()
+
+
+TWO_SWEEP_CASES = [(136, 75, 41), (64, 64, 64), (4, 5, 6), (8, 40, 7), (200, 33, 17), (68, 130, 30),
+                   (512, 62, 9), (132, 31, 3), (260, 94, 70)]
+
+
+@pytest.mark.parametrize("nx,ny,nz", TWO_SWEEP_CASES)
+def test_two_sweeps_in_one_pass_match_oracle(nx, ny, nz):
+    """stencil_apply2 (radius 1): S(S(u)) in one pass, against two oracle sweeps with a fixed
+    shell; ragged tiles in x and y (30-row tiles), short z, the shell and guard bands kept."""
+    torch = torch_cuda()
+    u = synth.uniform_field(nx, ny, nz, seed=4000 + nx + ny + nz)
+    c = np.random.default_rng(nx + nz).uniform(-1, 1, 2)
+    c = (c / np.sum(np.abs(c))).astype(np.float32)
+    plan = StencilPlan(nx, ny, nz, 1, c)
+    gin = Guarded(torch, u)
+    gout = Guarded(torch, u, fill_sentinel=True)
+    plan.apply2(gin.ptr, gout.ptr)
+    plan.status()
+    got = gout.numpy()
+    assert gin.guards_intact() and gout.guards_intact()
+    np.testing.assert_array_equal(gin.numpy(), u)
+    plan.close()
+    want = oracle.run_sweeps(u, c, 1, 2)
+    m = interior_mask(u.shape, 1)
+    if m.any():
+        assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= 2e-5 * float(np.max(np.abs(u)))
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD), "shell written"
+
+
+@pytest.mark.parametrize("nsweeps", [2, 5, 6, 9, 10])
+def test_radius1_sweep_loops_with_two_sweep_passes_match_oracle(nsweeps):
+    """stencil_sweeps at radius 1 runs 2*floor(n/4) two-sweep passes plus single sweeps; the
+    result lands in the buffer the sweep count says, and matches the oracle's loop."""
+    torch = torch_cuda()
+    nx, ny, nz = 200, 97, 45
+    u0 = synth.uniform_field(nx, ny, nz, seed=77)
+    c = np.float32([-0.5, 1.0 / 12.0])
+    plan = StencilPlan(nx, ny, nz, 1, c)
+    for use_graph in (False, True):
+        a = torch.from_numpy(u0.ravel()).cuda()
+        b = a.clone()
+        plan.sweeps(a, b, nsweeps, use_graph=use_graph)
+        plan.status(None, a)
+        got = (a if nsweeps % 2 == 0 else b).cpu().numpy().reshape(u0.shape)
+        want = oracle.run_sweeps(u0, c, 1, nsweeps)
+        m = interior_mask(u0.shape, 1)
+        assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= nsweeps * 1e-5 * float(np.max(np.abs(u0)))
+        np.testing.assert_array_equal(got[~m], u0[~m])
+    plan.close()
+
+
+def test_two_sweep_pass_only_for_radius_1():
+    torch = torch_cuda()
+    plan = StencilPlan(64, 64, 64, 4, synth.laplacian8_coeffs())
+    a = torch.zeros(64 ** 3, device="cuda")
+    b = torch.zeros(64 ** 3, device="cuda")
+    with pytest.raises(Exception) as ei:
+        plan.apply2(a, b)
+    assert "radius 1" in str(ei.value)
+    plan.close()

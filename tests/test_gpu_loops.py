@@ -55,11 +55,12 @@ def test_native_sweeps_match_oracle_run_sweeps(dims, R, nsweeps, use_graph):
     plan.close()
 
 
-@pytest.mark.parametrize("nsweeps", [1, 3])
+@pytest.mark.parametrize("nsweeps", [1, 3, 5])
 @pytest.mark.parametrize("dims,R", [((136, 75, 200), 4), ((64, 40, 140), 1), ((32, 32, 20), 4)])
 def test_host_buffer_sweeps_match_oracle(dims, R, nsweeps):
     """stencil_apply_host: one sweep runs pipelined over z-slabs on three streams, several
-    sweeps run back to back on the device; both from host to host."""
+    sweeps run back to back on the device (radius 1: four of five in two-sweep passes);
+    both from host to host."""
     torch_cuda()
     nx, ny, nz = dims
     c = unit_coeffs(R, 7)
