@@ -384,3 +384,38 @@ def test_two_sweep_pass_only_for_radius_1():
         plan.apply2(a, b)
     assert "radius 1" in str(ei.value)
     plan.close()
+
+
+def test_star7_lap_512_ten_sweeps_as_two_sweep_passes():
+    """The 10-sweep 512^3 7-point workload as five two-sweep passes (stencil_apply2).  Each
+    pass is checked on the GPU's own input v: with |S(w) - exact| <= 1e-5 sum|c| max|w| per
+    sweep, a pass is within 2e-5 (sum|c|)^2 max|v| of S(S(v)), at sampled points and on
+    three whole planes."""
+    torch = torch_cuda()
+    n = 512
+    u0 = synth.uniform_field(n, n, n)
+    c = synth.laplacian2_coeffs()
+    c32 = np.asarray(c, np.float32)
+    sc = float(np.sum(np.abs(c32)))
+    plan = StencilPlan(n, n, n, 1, c)
+    a = torch.from_numpy(u0.ravel()).cuda()
+    b = a.clone()
+    idx = sample_interior(u0.shape, 1, 200000, seed=5, planes=(1, 255, 510))
+    worst = 0.0
+    for k in range(5):
+        v = a.cpu().numpy().reshape(u0.shape)
+        plan.apply2(a, b)
+        plan.status(None, b)
+        s1 = oracle.apply(v, c32, 1)  # the first sweep, shell copied from v
+        want = oracle.apply_points(s1, c32, 1, idx)
+        got = b.cpu().numpy()[idx]
+        tol = 2e-5 * sc * sc * float(np.max(np.abs(v)))
+        err = float(np.max(np.abs(got.astype(np.float64) - want)))
+        assert err <= tol, f"pass {k}: {err} > {tol}"
+        worst = max(worst, err / tol)
+        a, b = b, a
+    host = a.cpu().numpy().reshape(u0.shape)
+    m = interior_mask(u0.shape, 1)
+    np.testing.assert_array_equal(host[~m], u0[~m])
+    plan.close()
+    print(f"star7 512^3 x10 as two-sweep passes: worst err/tol {worst:.3f}")
