@@ -54,7 +54,8 @@ SHAPES = [(512, 512, 512), (640, 640, 640), (1536, 1536, 256), (64, 64, 64), (13
 
 
 @pytest.mark.parametrize("nx,ny,nz", SHAPES)
-@pytest.mark.parametrize("R,kind,occ", [(4, 0, 2), (4, 1, 2), (1, 0, 4), (2, 0, 3), (3, 1, 2), (4, 3, 2)])
+@pytest.mark.parametrize("R,kind,occ", [(4, 0, 2), (4, 1, 2), (1, 0, 4), (2, 0, 3), (3, 1, 2), (4, 3, 2),
+                                        (4, 2, 2), (1, 4, 2)])
 @pytest.mark.parametrize("sms", [152, 148, 7])
 def test_choice_matches_a_scan_over_every_chunk_count(nx, ny, nz, R, kind, occ, sms):
     got = _lib.schedule_query(nx, ny, nz, R, kind, sms, occ)
@@ -83,10 +84,17 @@ def test_tall_grid_plans_quickly():
     assert got["tiles"] == 2 and got["zchunks"] >= 152 and got["grid"] == 304
 
 
+def test_two_sweep_kind_only_for_radius_1():
+    got = _lib.schedule_query(512, 512, 512, 1, 4, 152, 2)
+    assert got["tile_y"] == 30 and got["tiles"] == 8 * 17
+    with pytest.raises(_lib.StencilError):
+        _lib.schedule_query(512, 512, 512, 4, 4, 152, 2)
+
+
 def test_empty_interior_and_bad_arguments():
     got = _lib.schedule_query(8, 8, 8, 4, 0, 152, 2)
     assert got["grid"] == 0 and got["zchunks"] == 0
     for args in [(64, 64, 64, 0, 0, 152, 2), (64, 64, 64, 4, 4, 152, 2), (64, 64, 64, 4, 0, 0, 2),
-                 (64, 64, 64, 4, 0, 152, 0), (1 << 31, 4, 4, 4, 0, 152, 2)]:
+                 (64, 64, 64, 4, 0, 152, 0), (1 << 31, 4, 4, 4, 0, 152, 2), (64, 64, 64, 1, 5, 152, 2)]:
         with pytest.raises(_lib.StencilError):
             _lib.schedule_query(*args)
