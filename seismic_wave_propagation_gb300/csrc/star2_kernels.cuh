@@ -186,6 +186,16 @@ __global__ void __launch_bounds__(256, MINB)
       row_ok[k] = st2 && gy2[k] < p.ny - 1 && gx < p.nx;
     }
     const bool vec_ok = gx >= 1 && gx + 4 <= p.nx - 1;
+    // Which of this thread's first-sweep points lie on an x or y face (bit 4k + e; the
+    // extra column's point of row k: bit 8 + k): fixed for the whole item.
+    unsigned face = 0u;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (on_face(p, gx + e, gy1[k])) face |= 1u << (4 * k + e);
+      if (ext && on_face(p, gxe, gy1[k])) face |= 1u << (8 + k);
+    }
     for (int j = 0; j < L; ++j) {
       if (!mbar_wait_bounded(base + 8u * slot, phase)) fail(J);
       const float* pl = ring + slot * PSTRIDE;
@@ -202,20 +212,23 @@ __global__ void __launch_bounds__(256, MINB)
 
       // ---- stage 1: u1 at plane pz-1 is complete, write it --------------------------------
       if (j >= 2) {
-        const bool zface = pz - 1 == 0 || pz - 1 == p.nz - 1;
+        // Points on a face keep u0: the whole plane on a z face, else the masked points.
+        const unsigned keep = (pz - 1 == 0 || pz - 1 == p.nz - 1) ? 0x3FFu : face;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           P4 v = fma2x(c1, x[k], s1[0][k]);
+          if (keep) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (zface || on_face(p, gx + e, gy1[k])) pset(v, e, pget(xprev[k], e));
+            for (int e = 0; e < 4; ++e)
+              if (keep & (1u << (4 * k + e))) pset(v, e, pget(xprev[k], e));
+          }
           *reinterpret_cast<float4*>(u1w + w1 + k * BW) = tof4(v);
         }
         if (ext) {
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             float v = fmaf(c1.x, ex[k], es1[0][k]);
-            if (zface || on_face(p, gxe, gy1[k])) v = eprev[k];
+            if (keep & (1u << (8 + k))) v = eprev[k];
             u1w[(2 * tr + k) * BW + ecol] = v;
           }
         }

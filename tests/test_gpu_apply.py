@@ -336,7 +336,7 @@ def test_two_sweeps_in_one_pass_match_oracle(nx, ny, nz):
     torch = torch_cuda()
     u = synth.uniform_field(nx, ny, nz, seed=4000 + nx + ny + nz)
     c = np.random.default_rng(nx + nz).uniform(-1, 1, 2)
-    c = (c / np.sum(np.abs(c))).astype(np.float32)
+    c = (c / (abs(c[0]) + 6.0 * abs(c[1]))).astype(np.float32)  # max-norm gain 1
     plan = StencilPlan(nx, ny, nz, 1, c)
     gin = Guarded(torch, u)
     gout = Guarded(torch, u, fill_sentinel=True)
@@ -389,14 +389,15 @@ def test_two_sweep_pass_only_for_radius_1():
 def test_star7_lap_512_ten_sweeps_as_two_sweep_passes():
     """The 10-sweep 512^3 7-point workload as five two-sweep passes (stencil_apply2).  Each
     pass is checked on the GPU's own input v: with |S(w) - exact| <= 1e-5 sum|c| max|w| per
-    sweep, a pass is within 2e-5 (sum|c|)^2 max|v| of S(S(v)), at sampled points and on
-    three whole planes."""
+    sweep and S's max-norm gain g = |c0| + 6|c1|, a pass is within 2e-5 sum|c| g max|v| of
+    S(S(v)), at sampled points and on three whole planes."""
     torch = torch_cuda()
     n = 512
     u0 = synth.uniform_field(n, n, n)
     c = synth.laplacian2_coeffs()
     c32 = np.asarray(c, np.float32)
     sc = float(np.sum(np.abs(c32)))
+    gain = abs(float(c32[0])) + 6.0 * abs(float(c32[1]))
     plan = StencilPlan(n, n, n, 1, c)
     a = torch.from_numpy(u0.ravel()).cuda()
     b = a.clone()
@@ -409,7 +410,7 @@ def test_star7_lap_512_ten_sweeps_as_two_sweep_passes():
         s1 = oracle.apply(v, c32, 1)  # the first sweep, shell copied from v
         want = oracle.apply_points(s1, c32, 1, idx)
         got = b.cpu().numpy()[idx]
-        tol = 2e-5 * sc * sc * float(np.max(np.abs(v)))
+        tol = 2e-5 * sc * gain * float(np.max(np.abs(v)))
         err = float(np.max(np.abs(got.astype(np.float64) - want)))
         assert err <= tol, f"pass {k}: {err} > {tol}"
         worst = max(worst, err / tol)

@@ -76,7 +76,7 @@ def test_slab_sweeps_match_oracle(dims, R, P, nsweeps):
     torch = torch_cuda()
     nx, ny, nz = dims
     c = synth.laplacian8_coeffs()[:R + 1] if R == 4 else np.random.default_rng(R).uniform(-1, 1, R + 1)
-    c = (c / np.sum(np.abs(c))).astype(np.float32)
+    c = (c / (abs(c[0]) + 6.0 * np.sum(np.abs(c[1:])))).astype(np.float32)  # max-norm gain 1
     u0 = synth.uniform_field(nx, ny, nz, seed=42 + R)
     slabs = StencilSlabs(nx, ny, nz, R, c, P)
     a = to_slabs(torch, slabs, u0)
