@@ -593,6 +593,11 @@ def run_report_configs(args):
                 units, per = nsw, traffic.apply_bytes(nx, ny, nz, r)
             reps = max(1, min(101, int(2000 // max(1, units))))
             ms = _time_loop(loop, reps, 3, stream)
+            chained = None
+            if w["init"] != "wave" and units == 1 and nx * ny * nz <= 1 << 20:
+                # a single sweep of a small grid is launch-bound: also report its time when
+                # sweeps are chained back to back in one graph
+                chained = _time_loop(lambda: plan.sweeps(bufs[0], bufs[1], 1000, True, stream), 5, 2, stream) / 1000
             plan.status(stream)
         ms_unit = ms / units
         key = {"star25_lap8_512": ("star25_512", 0), "wave25_640": ("wave25_640", 1)}.get(name)
@@ -603,6 +608,10 @@ def run_report_configs(args):
                 "compulsory_bytes_per_point": per / interior,
                 "dram_bytes_per_point_ncu": dram / interior if dram else None,
                 "parity_max_err_over_tol": None, "timed_loops": reps}
+        if w["init"] != "wave":
+            line["sweep_path"] = plan.sweep_path
+        if chained is not None:
+            line["ms_per_sweep_chained_1000_in_one_graph"] = chained
         if not args.skip_cpu:
             # The CPU-oracle leg: the workload's first sweep or step checked against the
             # oracle at sampled points, then the oracle timed on a bounded sample.

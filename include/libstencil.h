@@ -46,6 +46,11 @@ extern "C" {
 
 #define STENCIL_MAX_RADIUS 4
 
+/* Sweep paths (stencil_plan_set_sweep_path). */
+#define STENCIL_PATH_AUTO 0   /* chosen by grid size (the default) */
+#define STENCIL_PATH_STAGED 1 /* the 2.5D kernel: TMA-staged planes, z window in registers */
+#define STENCIL_PATH_DIRECT 2 /* the direct-load kernel: operands read straight from memory */
+
 typedef struct stencil_plan stencil_plan; /* opaque */
 
 /*
@@ -70,9 +75,34 @@ void stencil_plan_destroy(stencil_plan* plan);
  * Callers wanting the shell copied (a "fixed boundary") pre-copy `in` into `out` once;
  * ping-pong sweeps that start from two copies of the same field keep it fixed.
  *  in, out   device pointers to nx*ny*nz floats, 16-byte aligned, must not overlap.
+ * The sweep runs on the plan's sweep path (stencil_plan_set_sweep_path).
  * Errors: STENCIL_ERR_ARG, _ALIGNMENT, _ALIAS, _CUDA.
  */
 int stencil_apply(stencil_plan* plan, const float* in, float* out, void* stream);
+
+/*
+ * Which kernel computes the plan's sweeps (stencil_apply, the sweep loops and host-buffer
+ * sweeps, the slabs of stencil_slabs_apply; not stencil_apply_semi or stencil_apply2):
+ *  STENCIL_PATH_STAGED  the 2.5D kernel: each x-y tile plus its halo staged plane by plane
+ *                       in shared memory by TMA, the z window held in registers; reads
+ *                       each point from DRAM about once; the fast path on large grids.
+ *  STENCIL_PATH_DIRECT  one thread per four x points of an interior row, every operand a
+ *                       128-bit load from global memory; no staging and no waits.  On
+ *                       small grids its launch-to-finish time is well below the staged
+ *                       kernel's (GB300, one sweep launched after another: 64^3 radius 1
+ *                       4.1 against 6.2 us, radius 4 4.1 against 8.2 us).
+ *  STENCIL_PATH_AUTO    (the default) single sweeps on the direct kernel up to 100, 12, 5
+ *                       and 3.5 million grid points for radius 1, 2, 3 and 4, on the
+ *                       staged one above.
+ * Both compute the same sweep up to fp32 rounding order.  Radius-1 loops (stencil_sweeps,
+ * stencil_apply_host with nsweeps > 1) run most sweeps as two-sweep passes
+ * (stencil_apply2) on the staged path, and on the automatic path from 7 million points,
+ * where a pass beats two direct sweeps; their other sweeps run on the plan's sweep path,
+ * and the direct path runs none as passes.  stencil_debug_inject affects only the staged
+ * kernels.  Returns STENCIL_OK, or STENCIL_ERR_ARG for a NULL plan or a path outside
+ * [0, 2].
+ */
+int stencil_plan_set_sweep_path(stencil_plan* plan, int path);
 
 /*
  * Two sweeps in one pass: out = S(S(in)) for the plan's stencil S (temporal blocking of
@@ -206,8 +236,11 @@ int wave_run_host(stencil_plan* plan, float* u_prev_host, float* u_host,
  * 2 = the no-eta kernel of wave_step_pml's inner region, over the whole grid,
  * 3 = stencil_apply_semi, 4 = stencil_apply2 (radius 1 only)), written
  * to info[0..n): grid CTAs, threads per CTA, dynamic shared bytes, CTAs resident per
- * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count.
- * Returns the number of values written, or a negative error code.
+ * SM, x-y tiles, z-chunks, tile width, tile height, pipeline stages, SM count, and the
+ * sweep path (STENCIL_PATH_STAGED or _DIRECT; kind 0 on a direct plan reports its blocks,
+ * 256 threads, no shared memory, blocks per SM, 0 tiles and chunks, a 4 x 1 "tile" and 0
+ * stages).  At most 11 values.  Returns the number of values written, or a negative error
+ * code.
  */
 int stencil_plan_launch_info(const stencil_plan* plan, int kind, int64_t* info, int n);
 
@@ -248,8 +281,9 @@ int stencil_debug_inject(stencil_plan* plan, int mode);
  * cannot call cudaMalloc when they need a sweep (for example code running inside another
  * framework's memory pool that owns the free device memory, or a process whose device
  * memory footprint is fixed at start-up).  It computes exactly what
- * stencil_plan_create + stencil_apply compute, with the same arguments, restrictions and
- * error codes, and allocates nothing: no cudaMalloc/cudaFree, no heap, no plan.
+ * stencil_plan_create + stencil_apply compute (on the automatic sweep path), with the same
+ * arguments, restrictions and error codes, and allocates nothing: no cudaMalloc/cudaFree,
+ * no heap, no plan.
  *
  * Scratch: the kernel's 16-byte status block lives in a file-scope device array of 256
  * bytes that every GPU which loads the library holds until the process exits.  The need

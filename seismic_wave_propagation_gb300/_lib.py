@@ -23,7 +23,8 @@ ERRORS = {-1: "STENCIL_ERR_ARG", -2: "STENCIL_ERR_ALIGNMENT", -3: "STENCIL_ERR_A
           -4: "STENCIL_ERR_CUDA", -5: "STENCIL_ERR_TIMEOUT"}
 KIND_APPLY, KIND_WAVE, KIND_WAVE_PML, KIND_SEMI, KIND_APPLY2 = 0, 1, 2, 3, 4
 LAUNCH_INFO_KEYS = ("grid", "threads", "smem", "ctas_per_sm", "tiles", "zchunks", "tile_x",
-                    "tile_y", "stages", "sms")
+                    "tile_y", "stages", "sms", "path")
+SWEEP_PATHS = {"auto": 0, "staged": 1, "direct": 2}
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,7 @@ def load():
         lib.wave_run_host.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
         lib.stencil_plan_launch_info.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int]
         lib.stencil_debug_inject.argtypes = [vp, ctypes.c_int]
+        lib.stencil_plan_set_sweep_path.argtypes = [vp, ctypes.c_int]
         lib.wave_eta_stencil.argtypes = [vp, vp, vp, ctypes.c_float, ctypes.c_float, vp]
         lib.stencil_plan_host_phases.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         lib.stencil_schedule_query.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -84,7 +86,7 @@ def load():
         lib.stencil_slabs_wave_step.argtypes = [vp] * 7
         lib.stencil_slabs_status.argtypes = [vp, vp]
         for fn in ("stencil_apply", "stencil_apply_semi", "stencil_apply2", "wave_step", "wave_step_pml", "stencil_sweeps", "wave_steps",
-                   "stencil_plan_status", "stencil_apply_host",
+                   "stencil_plan_status", "stencil_apply_host", "stencil_plan_set_sweep_path",
                    "wave_run_host", "stencil_plan_launch_info", "stencil_debug_inject",
                    "stencil_schedule_query", "stencil_plan_host_phases", "wave_eta_stencil", "stencil_slabs_extent",
                    "stencil_slabs_exchange", "stencil_slabs_apply", "stencil_slabs_wave_step",
@@ -221,6 +223,15 @@ class StencilPlan:
         n = self.npoints
         _check(self._lib.wave_run_host(self._p, _host(u_prev, n), _host(u, n), _host(v2dt2, n),
                                        _host(eta, n), int(nsteps), _stream(stream)))
+
+    def set_sweep_path(self, path) -> None:
+        """stencil_plan_set_sweep_path: "auto", "staged" or "direct" (or 0, 1, 2)."""
+        _check(self._lib.stencil_plan_set_sweep_path(self._p, SWEEP_PATHS.get(path, path)))
+
+    @property
+    def sweep_path(self) -> str:
+        """The kernel the plan's sweeps run on: "staged" or "direct"."""
+        return {1: "staged", 2: "direct"}[self.launch_info(KIND_APPLY)["path"]]
 
     def launch_info(self, kind: int = KIND_APPLY) -> dict:
         buf = (ctypes.c_int64 * len(LAUNCH_INFO_KEYS))()

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "direct_kernels.cuh"
 #include "star2_kernels.cuh"
 #include "star_kernels.cuh"
 
@@ -77,5 +78,10 @@ KernelDesc apply_kernel_desc(int radius);
 KernelDesc apply2_kernel_desc(int radius);
 KernelDesc semi_kernel_desc(int radius);
 KernelDesc wave_kernel_desc(int radius, bool noeta);
+// The direct-load sweep for small grids (direct_kernels.cuh), radius 1..4: its entry (for
+// attributes and occupancy) and its launch with 256 threads per block.
+const void* direct_kernel_fn(int radius);
+cudaError_t launch_direct(int radius, dim3 grid, cudaStream_t stream, const DirectParams& p);
+constexpr int kDirectThreads = 256;
 
 }  // namespace libstencil

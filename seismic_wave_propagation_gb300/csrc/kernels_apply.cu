@@ -36,4 +36,24 @@ KernelDesc semi_kernel_desc(int radius) {
   }
 }
 
+// Direct-load sweeps (small grids).
+const void* direct_kernel_fn(int radius) {
+  switch (radius) {
+    case 1: return (const void*)star_direct_kernel<1>;
+    case 2: return (const void*)star_direct_kernel<2>;
+    case 3: return (const void*)star_direct_kernel<3>;
+    default: return (const void*)star_direct_kernel<4>;
+  }
+}
+
+cudaError_t launch_direct(int radius, dim3 grid, cudaStream_t stream, const DirectParams& p) {
+  switch (radius) {
+    case 1: star_direct_kernel<1><<<grid, kDirectThreads, 0, stream>>>(p); break;
+    case 2: star_direct_kernel<2><<<grid, kDirectThreads, 0, stream>>>(p); break;
+    case 3: star_direct_kernel<3><<<grid, kDirectThreads, 0, stream>>>(p); break;
+    default: star_direct_kernel<4><<<grid, kDirectThreads, 0, stream>>>(p); break;
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace libstencil

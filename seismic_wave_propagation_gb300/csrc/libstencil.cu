@@ -98,6 +98,11 @@ struct stencil_plan {
   int reg_kind;            // 2: inner and band; 1: no inner region (one full launch)
   StarParams reg_inner, reg_band;
   int reg_inner_grid, reg_band_grid;
+  // Sweep path of stencil_apply and the sweep loops: STENCIL_PATH_AUTO (chosen by grid
+  // size), _STAGED or _DIRECT; `direct` is the resolved choice.
+  int sweep_path;
+  bool direct;
+  int direct_occupancy;  // blocks of the direct kernel per SM
 };
 
 namespace {
@@ -357,12 +362,61 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
   return STENCIL_OK;
 }
 
+// Grids up to this many points (per radius) sweep faster with the direct-load kernel than
+// with the staged one: there the launch and pipeline-filling latency of the staged kernel
+// outweighs its saving in loads.  Measured on GB300, one sweep launched after another, on
+// cubes: radius 1 direct faster through 448^3 (136 against 149 us), slower at 512^3;
+// radius 2 through 224^3, slower at 256^3; radius 3 through 160^3, slower at 192^3;
+// radius 4 through 144^3 (12.3 against 14.4 us), slower at 160^3.
+constexpr int64_t kDirectMaxPoints[STENCIL_MAX_RADIUS + 1] = {0, 100000000, 12000000, 5000000, 3500000};
+// Radius-1 loops on the automatic path: from this many points a two-sweep pass of the
+// staged kernel beats two direct sweeps (GB300, chained in a graph: 192^3 10.96 against
+// 10.59 us per sweep, 256^3 21.5 against 26.9).
+constexpr int64_t kPairMinPoints = 7000000;
+
+bool resolve_direct(const stencil_plan* p) {
+  if (p->sweep_path == STENCIL_PATH_DIRECT) return true;
+  if (p->sweep_path == STENCIL_PATH_STAGED) return false;
+  return npoints(p) <= kDirectMaxPoints[p->radius];
+}
+
+// Geometry of a direct-kernel sweep over output planes [R + zoff, R + zoff + nzi).
+DirectParams direct_params(const stencil_plan* p, const float* in, float* out, int zoff, int nzi,
+                           int64_t& blocks) {
+  const int R = p->radius;
+  DirectParams d{};
+  d.in = in;
+  d.out = out;
+  d.nx = (int)p->nx;
+  d.ny = (int)p->ny;
+  d.z0 = R + zoff;
+  d.q0 = R >> 2;                                   // first float4 column with x >= R
+  d.nq = (int)(((p->nx - R - 1) >> 2) + 1) - d.q0;  // through the column with x = nx - R - 1
+  d.nyi = (int)(p->ny - 2 * R);
+  d.total = interior_empty(p) || nzi <= 0 ? 0 : (int64_t)d.nq * d.nyi * nzi;
+  for (int r = 0; r <= STENCIL_MAX_RADIUS; ++r) d.c[r] = p->c[r];
+  blocks = (d.total + kDirectThreads - 1) / kDirectThreads;
+  return d;
+}
+
+int launch_direct_sweep(stencil_plan* p, const float* in, float* out, cudaStream_t stream, int zoff,
+                        int nzi) {
+  if (nzi < 0) nzi = (int)(p->nz - 2 * p->radius);
+  int64_t blocks = 0;
+  const DirectParams d = direct_params(p, in, out, zoff, nzi, blocks);
+  if (blocks == 0) return STENCIL_OK;  // empty interior: nothing to do
+  if (blocks > INT32_MAX) return fail(STENCIL_ERR_ARG, "grid too large for the direct sweep");
+  cudaError_t e = launch_direct(p->radius, dim3((unsigned)blocks), stream, d);
+  return e == cudaSuccess ? STENCIL_OK : cuda_fail(e, "kernel launch");
+}
+
 // Launch one sweep (kind 0, 3) or wave step (1; 2 = without eta).  nzi >= 0 restricts it
 // to the output planes [R + zoff, R + zoff + nzi); `geo` (with `geo_grid` CTAs) gives the
 // work of the launch explicitly.
 int launch(stencil_plan* p, int kind, const float* u, const float* uprev, const float* v2dt2,
            const float* eta, float* out, cudaStream_t stream, int zoff = 0, int nzi = -1,
            const StarParams* geo = nullptr, int geo_grid = 0) {
+  if (kind == 0 && p->direct && !geo) return launch_direct_sweep(p, u, out, stream, zoff, nzi);
   StarParams sp = geo ? *geo : p->params[kind];
   int grid = geo ? geo_grid : p->grid[kind];
   if (!geo && nzi >= 0) geometry(p, kind, zoff, nzi, sp, grid);
@@ -570,11 +624,18 @@ int wave_step_regions(stencil_plan* p, const float* u_prev, const float* u, floa
 }
 
 // `n` ping-pong sweeps x -> y -> x ... on stream s.  Where the plan has the two-sweep
-// kernel (radius 1) most of them run in pairs, one pass per pair; the number of such
-// passes is kept even so that the result lands where n single sweeps would leave it
-// (x for even n, y for odd n): 2*floor(n/4) passes, then the rest one by one.
+// kernel (radius 1), most of them run in pairs, one pass per pair, on the staged path and,
+// on the automatic path, from kPairMinPoints up (below, two direct sweeps are faster);
+// the number of such passes is kept even so that the result lands where n single sweeps
+// would leave it (x for even n, y for odd n): 2*floor(n/4) passes, then the rest one by
+// one on the plan's sweep path.
+bool loop_pairs(const stencil_plan* p) {
+  if (!p->kd[4].fn || p->sweep_path == STENCIL_PATH_DIRECT) return false;
+  return p->sweep_path == STENCIL_PATH_STAGED || npoints(p) >= kPairMinPoints;
+}
+
 int ping_pong(stencil_plan* p, float* x, float* y, int n, cudaStream_t s) {
-  const int pairs = p->kd[4].fn ? 2 * (n / 4) : 0;
+  const int pairs = loop_pairs(p) ? 2 * (n / 4) : 0;
   for (int i = 0; i < pairs; ++i) {
     const int r = launch(p, 4, x, nullptr, nullptr, nullptr, y, s);
     if (r) return r;
@@ -656,6 +717,15 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
     }
     plan_geometry(p, k);
   }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p->direct_occupancy, direct_kernel_fn(radius),
+                                                    kDirectThreads, 0);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "kernel attributes");
+    stencil_plan_destroy(p);
+    return nullptr;
+  }
+  p->sweep_path = STENCIL_PATH_AUTO;
+  p->direct = resolve_direct(p);
   return p;
 }
 
@@ -771,7 +841,7 @@ int stencil_sweeps(stencil_plan* p, float* a, float* b, int nsweeps, int use_gra
   if ((rc = check_field(p, a, "a")) || (rc = check_field(p, b, "b"))) return rc;
   if (overlap(a, b, (size_t)npoints(p) * 4)) return fail(STENCIL_ERR_ALIAS, "a and b overlap");
   const uint64_t key[8] = {1, (uint64_t)(uintptr_t)a, (uint64_t)(uintptr_t)b, (uint64_t)nsweeps,
-                           (uint64_t)p->debug_mode, 0, 0, 0};
+                           (uint64_t)p->debug_mode, (uint64_t)p->sweep_path, 0, 0};
   return run_loop(p, key, use_graph != 0, static_cast<cudaStream_t>(stream),
                   [&](cudaStream_t s) { return ping_pong(p, a, b, nsweeps, s); });
 }
@@ -895,9 +965,16 @@ int stencil_plan_launch_info(const stencil_plan* p, int kind, int64_t* info, int
   if (!p->kd[kind].fn) return fail(STENCIL_ERR_ARG, "kind %d is not built for radius %d", kind, p->radius);
   const KernelDesc& kd = p->kd[kind];
   const StarParams& sp = p->params[kind];
-  const int64_t v[10] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.box[0].ntiles,
-                         sp.box[0].nchunks, kTX,    kd.tile_y, kd.stages,       p->num_sms};
-  const int m = std::min(n, 10);
+  int64_t v[11] = {p->grid[kind], kd.threads, kd.smem, p->occupancy[kind], sp.box[0].ntiles,
+                   sp.box[0].nchunks, kTX,    kd.tile_y, kd.stages,       p->num_sms, STENCIL_PATH_STAGED};
+  if (kind == 0 && p->direct) {  // one thread per 4 x points of an interior row; no tiles or chunks
+    int64_t blocks = 0;
+    direct_params(p, nullptr, nullptr, 0, (int)(p->nz - 2 * p->radius), blocks);
+    const int64_t d[11] = {blocks, kDirectThreads, 0, p->direct_occupancy, 0, 0, 4, 1, 0, p->num_sms,
+                           STENCIL_PATH_DIRECT};
+    std::copy(d, d + 11, v);
+  }
+  const int m = std::min(n, 11);
   for (int i = 0; i < m; ++i) info[i] = v[i];
   return m;
 }
@@ -940,6 +1017,15 @@ int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int k
   const int k = std::min(n, 7);
   for (int i = 0; i < k; ++i) info[i] = v[i];
   return k;
+}
+
+int stencil_plan_set_sweep_path(stencil_plan* p, int path) {
+  if (!p) return fail(STENCIL_ERR_ARG, "plan is NULL");
+  if (path < STENCIL_PATH_AUTO || path > STENCIL_PATH_DIRECT)
+    return fail(STENCIL_ERR_ARG, "sweep path %d is not one of 0 (auto), 1 (staged), 2 (direct)", path);
+  p->sweep_path = path;
+  p->direct = resolve_direct(p);
+  return STENCIL_OK;
 }
 
 int stencil_debug_inject(stencil_plan* p, int mode) {
@@ -1014,6 +1100,8 @@ extern "C" int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int rad
   if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
   if (pl.occupancy[0] < 1) return fail(STENCIL_ERR_CUDA, "kernel cannot be resident (occupancy 0)");
   plan_geometry(&pl, 0);
+  pl.sweep_path = STENCIL_PATH_AUTO;
+  pl.direct = resolve_direct(&pl);
 
   if ((rc = check_field(&pl, in, "in")) || (rc = check_field(&pl, out, "out"))) return rc;
   if (overlap(in, out, (size_t)npoints(&pl) * 4)) return fail(STENCIL_ERR_ALIAS, "in and out overlap");

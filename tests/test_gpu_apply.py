@@ -9,9 +9,12 @@ from gpu_util import Guarded, interior_mask, sample_interior, sweep_tol, torch_c
 pytestmark = pytest.mark.gpu
 
 
-def run_apply(torch, u, coeffs, R, shell_from_input=False):
+def run_apply(torch, u, coeffs, R, shell_from_input=False, path=None):
     nz, ny, nx = u.shape
     plan = StencilPlan(nx, ny, nz, R, coeffs)
+    if path is not None:
+        plan.set_sweep_path(path)
+        assert plan.sweep_path == path
     gin = Guarded(torch, u)
     gout = Guarded(torch, u, fill_sentinel=not shell_from_input)
     plan.apply(gin.ptr, gout.ptr)
@@ -45,13 +48,44 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("path", ["staged", "direct"])
 @pytest.mark.parametrize("nx,ny,nz,R", CASES)
-def test_apply_matches_oracle(nx, ny, nz, R):
+def test_apply_matches_oracle(nx, ny, nz, R, path):
+    """Both sweep kernels on the same ragged grids (the automatic choice takes the direct
+    one for all of them)."""
     torch = torch_cuda()
     u = synth.uniform_field(nx, ny, nz, seed=1000 + nx + R)
     c = np.random.default_rng(R).uniform(-1, 1, R + 1)
-    out = run_apply(torch, u, c, R)
+    out = run_apply(torch, u, c, R, path=path)
     check(u, out, c, R)
+
+
+@pytest.mark.parametrize("dims,R,want", [((64, 64, 64), 1, "direct"), ((448, 448, 448), 1, "direct"),
+                                         ((480, 480, 480), 1, "staged"), ((224, 224, 224), 2, "direct"),
+                                         ((232, 232, 232), 2, "staged"), ((168, 168, 168), 3, "direct"),
+                                         ((172, 172, 172), 3, "staged"), ((148, 148, 148), 4, "direct"),
+                                         ((152, 152, 152), 4, "staged"), ((512, 512, 512), 4, "staged")])
+def test_automatic_sweep_path(dims, R, want):
+    """The automatic choice: the direct kernel up to 100, 12, 5 and 3.5 million points for
+    radius 1..4; launch_info reports the chosen kernel's launch."""
+    torch_cuda()
+    plan = StencilPlan(*dims, R, np.ones(R + 1, np.float32))
+    assert plan.sweep_path == want
+    info = plan.launch_info(0)
+    if want == "direct":
+        nx, ny, nz = dims
+        cols = ((nx - R - 1) >> 2) + 1 - (R >> 2)
+        assert info["grid"] == -(-cols * (ny - 2 * R) * (nz - 2 * R) // 256)
+        assert (info["threads"], info["smem"], info["tiles"], info["zchunks"]) == (256, 0, 0, 0)
+    else:
+        assert info["smem"] > 0 and info["tiles"] > 0
+    plan.set_sweep_path("staged" if want == "direct" else "direct")
+    assert plan.sweep_path != want
+    plan.set_sweep_path("auto")
+    assert plan.sweep_path == want
+    with pytest.raises(Exception):
+        plan.set_sweep_path(3)
+    plan.close()
 
 
 @pytest.mark.parametrize("R", [1, 4])
@@ -78,10 +112,11 @@ def test_several_items_per_cta(nx, ny, nz, R):
     u = synth.uniform_field(nx, ny, nz, seed=3000 + R)
     c = np.random.default_rng(20 + R).uniform(-1, 1, R + 1)
     plan = StencilPlan(nx, ny, nz, R, c)
+    plan.set_sweep_path("staged")
     info = plan.launch_info(0)
     assert info["tiles"] * info["zchunks"] > info["grid"], info  # several items per CTA
     plan.close()
-    out = run_apply(torch, u, c, R)
+    out = run_apply(torch, u, c, R, path="staged")
     check(u, out, c, R)
 
 
@@ -231,12 +266,14 @@ def test_launch_geometry():
 
 @pytest.mark.parametrize("use_graph", [False, True])
 @pytest.mark.parametrize("nsweeps", [3, 4])
-def test_native_sweep_loop_matches_launch_by_launch(use_graph, nsweeps):
+@pytest.mark.parametrize("path", ["staged", "direct"])
+def test_native_sweep_loop_matches_launch_by_launch(use_graph, nsweeps, path):
     torch = torch_cuda()
     nx, ny, nz, R = 136, 75, 41, 4
     c = synth.laplacian8_coeffs()
     u = synth.uniform_field(nx, ny, nz)
     plan = StencilPlan(nx, ny, nz, R, c)
+    plan.set_sweep_path(path)
     a = torch.from_numpy(u.ravel()).cuda()
     b = a.clone()
     ra, rb = a.clone(), a.clone()
@@ -255,14 +292,17 @@ def test_native_sweep_loop_matches_launch_by_launch(use_graph, nsweeps):
     plan.close()
 
 
+@pytest.mark.parametrize("path", ["staged", "direct"])
 @pytest.mark.parametrize("dims,R", [((136, 75, 200), 4), ((64, 40, 140), 1), ((32, 32, 20), 4)])
-def test_pipelined_host_sweep_matches_device_path(dims, R):
-    """One host-to-host sweep runs pipelined over z-slabs; it must equal the device path."""
+def test_pipelined_host_sweep_matches_device_path(dims, R, path):
+    """One host-to-host sweep runs pipelined over z-slabs (each slab a z-range launch of
+    the plan's sweep kernel); it must equal the device path."""
     torch = torch_cuda()
     nx, ny, nz = dims
     c = synth.laplacian8_coeffs()[:R + 1] if R == 4 else synth.laplacian2_coeffs()
     u = synth.uniform_field(nx, ny, nz, seed=77)
     plan = StencilPlan(nx, ny, nz, R, c)
+    plan.set_sweep_path(path)
     out_h = np.full_like(u, 3.0)
     for _ in range(2):
         plan.apply_host(u, out_h, 1)
@@ -353,15 +393,18 @@ def test_two_sweeps_in_one_pass_match_oracle(nx, ny, nz):
     assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD), "shell written"
 
 
+@pytest.mark.parametrize("path", ["staged", "direct"])
 @pytest.mark.parametrize("nsweeps", [2, 5, 6, 9, 10])
-def test_radius1_sweep_loops_with_two_sweep_passes_match_oracle(nsweeps):
-    """stencil_sweeps at radius 1 runs 2*floor(n/4) two-sweep passes plus single sweeps; the
-    result lands in the buffer the sweep count says, and matches the oracle's loop."""
+def test_radius1_sweep_loops_with_two_sweep_passes_match_oracle(nsweeps, path):
+    """stencil_sweeps at radius 1 on the staged path runs 2*floor(n/4) two-sweep passes plus
+    single sweeps, on the direct path n single sweeps; the result lands in the buffer the
+    sweep count says, and matches the oracle's loop."""
     torch = torch_cuda()
     nx, ny, nz = 200, 97, 45
     u0 = synth.uniform_field(nx, ny, nz, seed=77)
     c = np.float32([-0.5, 1.0 / 12.0])
     plan = StencilPlan(nx, ny, nz, 1, c)
+    plan.set_sweep_path(path)
     for use_graph in (False, True):
         a = torch.from_numpy(u0.ravel()).cuda()
         b = a.clone()
@@ -420,3 +463,25 @@ def test_star7_lap_512_ten_sweeps_as_two_sweep_passes():
     np.testing.assert_array_equal(host[~m], u0[~m])
     plan.close()
     print(f"star7 512^3 x10 as two-sweep passes: worst err/tol {worst:.3f}")
+
+
+def test_sweep_path_change_recaptures_the_loop_graph():
+    """The cached graph of stencil_sweeps belongs to one sweep path: after a change of path
+    the next call captures the new kernel's loop, and both results match the oracle."""
+    torch = torch_cuda()
+    nx, ny, nz, R = 96, 50, 40, 2
+    u0 = synth.uniform_field(nx, ny, nz, seed=5)
+    c = np.float32([0.4, 0.05, -0.025])
+    plan = StencilPlan(nx, ny, nz, R, c)
+    want = oracle.run_sweeps(u0, c, R, 3)
+    m = interior_mask(u0.shape, R)
+    for path in ("direct", "staged", "direct"):
+        plan.set_sweep_path(path)
+        a = torch.from_numpy(u0.ravel()).cuda()
+        b = a.clone()
+        plan.sweeps(a, b, 3, use_graph=True)
+        plan.status(None, a)
+        got = b.cpu().numpy().reshape(u0.shape)
+        assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= 3e-5 * float(np.max(np.abs(u0)))
+        np.testing.assert_array_equal(got[~m], u0[~m])
+    plan.close()

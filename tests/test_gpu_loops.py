@@ -29,16 +29,21 @@ def unit_coeffs(R, seed):
     return (c / (abs(c[0]) + 6.0 * np.sum(np.abs(c[1:])))).astype(np.float32)
 
 
+@pytest.mark.parametrize("path", ["staged", "auto"])
 @pytest.mark.parametrize("use_graph", [True, False])
 @pytest.mark.parametrize("nsweeps", [3, 4])
 @pytest.mark.parametrize("dims,R", [((136, 75, 41), 4), ((200, 33, 57), 1), ((68, 130, 30), 2),
-                                    ((256, 96, 70), 3)])
-def test_native_sweeps_match_oracle_run_sweeps(dims, R, nsweeps, use_graph):
+                                    ((256, 96, 70), 3), ((256, 256, 128), 1)])
+def test_native_sweeps_match_oracle_run_sweeps(dims, R, nsweeps, use_graph, path):
+    """On the staged path and on the automatic one: the direct kernel at these sizes, and
+    at 256 x 256 x 128 (radius 1, above 7 million points) two-sweep passes with the odd
+    sweeps on the direct kernel."""
     torch = torch_cuda()
     nx, ny, nz = dims
     c = unit_coeffs(R, nx + R)
     u0 = synth.uniform_field(nx, ny, nz, seed=500 + R)
     plan = StencilPlan(nx, ny, nz, R, c)
+    plan.set_sweep_path(path)
     a = torch.from_numpy(u0.ravel()).cuda()
     b = a.clone()
     for _ in range(2):  # the second call replays the cached graph

@@ -1,6 +1,6 @@
-"""Seeded random grid shapes against the oracle: every radius, both ring protocols (radius 4
-meets at a CTA barrier, radii 1-3 release slots warp by warp), the semi-stencil sweep and
-the wave step, on sizes that are ragged in every axis (partial x and y tiles, short and
+"""Seeded random grid shapes against the oracle: every radius, both ring protocols of the
+staged sweep (radius 4 meets at a CTA barrier, radii 1-3 release slots warp by warp), the
+direct-load sweep, the semi-stencil sweep and the wave step, on sizes that are ragged in every axis (partial x and y tiles, short and
 uneven z-chunks, empty interiors)."""
 import numpy as np
 import pytest
@@ -28,16 +28,18 @@ SWEEP_SHAPES = shapes(2024, 24)
 WAVE_SHAPES = shapes(2025, 10)
 
 
-@pytest.mark.parametrize("semi", [False, True])
+@pytest.mark.parametrize("kernel", ["staged", "direct", "semi"])
 @pytest.mark.parametrize("nx,ny,nz,R", SWEEP_SHAPES)
-def test_random_shape_sweep(nx, ny, nz, R, semi):
+def test_random_shape_sweep(nx, ny, nz, R, kernel):
     torch = torch_cuda()
     u = synth.uniform_field(nx, ny, nz, seed=nx * 7 + ny * 11 + nz * 13 + R)
     c = np.random.default_rng(nx + ny + nz).uniform(-1, 1, R + 1)
     plan = StencilPlan(nx, ny, nz, R, c)
+    if kernel != "semi":
+        plan.set_sweep_path(kernel)
     gin = Guarded(torch, u)
     gout = Guarded(torch, u, fill_sentinel=True)
-    (plan.apply_semi if semi else plan.apply)(gin.ptr, gout.ptr)
+    (plan.apply_semi if kernel == "semi" else plan.apply)(gin.ptr, gout.ptr)
     plan.status()
     got = gout.numpy()
     assert gin.guards_intact() and gout.guards_intact()

@@ -20,8 +20,9 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("nx,ny,nz,R,coeffs", [
-    (136, 75, 41, 4, "laplacian8"),
-    (64, 64, 64, 1, "average7"),
+    (136, 75, 41, 4, "laplacian8"),    # the direct sweep (the automatic path of this size)
+    (64, 64, 64, 1, "average7"),       # the direct sweep
+    (256, 256, 160, 4, "laplacian8"),  # the staged sweep
 ])
 def test_noalloc_matches_oracle_and_plan_apply_twice(nx, ny, nz, R, coeffs):
     torch = torch_cuda()
