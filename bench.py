@@ -421,14 +421,17 @@ def run_ours(args, dist, rank, local, world):
 
 
 def run_profile_case(kind: str):
-    """Three launches of the 512^3 case of one kernel: the driver for ncu captures."""
+    """Three launches of the 512^3 case of one kernel (the 64^3 smoothing sweep for
+    "direct64", on the direct-load kernel): the driver for ncu captures."""
     import torch
     from seismic_wave_propagation_gb300 import StencilPlan
-    n = NX
-    r = 1 if kind in ("sweep7", "sweep7x2") else R
-    c = synth.laplacian2_coeffs() if r == 1 else synth.laplacian8_coeffs()
+    n = 64 if kind == "direct64" else NX
+    r = 1 if kind in ("sweep7", "sweep7x2", "direct64") else R
+    c = synth.average7_coeffs() if kind == "direct64" else synth.laplacian2_coeffs() if r == 1 else synth.laplacian8_coeffs()
     plan = StencilPlan(n, n, n, r, c)
-    if kind in ("sweep", "semi", "sweep7", "sweep7x2"):
+    if kind == "direct64":
+        plan.set_sweep_path("direct")
+    if kind in ("sweep", "semi", "sweep7", "sweep7x2", "direct64"):
         u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
         o = u.clone()
         fn = {"semi": plan.apply_semi, "sweep7x2": plan.apply2}.get(kind, plan.apply)
@@ -444,7 +447,7 @@ def run_profile_case(kind: str):
                 plan.wave_step(f[0], f[1], nxt, f[2], f[3])
     torch.cuda.synchronize()
     plan.status()
-    k = {"sweep": 0, "sweep7": 0, "wave": 1, "wave_inner": 2, "semi": 3, "sweep7x2": 4}[kind]
+    k = {"sweep": 0, "sweep7": 0, "direct64": 0, "wave": 1, "wave_inner": 2, "semi": 3, "sweep7x2": 4}[kind]
     print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info(k)}))
 
 
@@ -684,9 +687,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
-    ap.add_argument("--profile", choices=["sweep", "sweep7", "sweep7x2", "wave", "wave_inner", "semi"],
+    ap.add_argument("--profile", choices=["sweep", "sweep7", "sweep7x2", "wave", "wave_inner", "semi", "direct64"],
                     help="run 3 launches of the 512^3 case (ncu driver); sweep7 is the 7-point Laplacian, "
-                         "sweep7x2 its two-sweep pass, wave_inner the band step with no band (no-eta kernel)")
+                         "sweep7x2 its two-sweep pass, wave_inner the band step with no band (no-eta kernel), "
+                         "direct64 the 64^3 smoothing sweep on the direct-load kernel")
     ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
     if args.profile or args.report_configs:

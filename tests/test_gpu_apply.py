@@ -315,7 +315,8 @@ def test_pipelined_host_sweep_matches_device_path(dims, R, path):
 
 
 def test_grid_beyond_2pow31_points():
-    """64-bit indexing: 2048 x 1024 x 1030 = 2.16e9 points (8.6 GB per field)."""
+    """64-bit indexing: 2048 x 1024 x 1030 = 2.16e9 points (8.6 GB per field), on both
+    sweep kernels (the direct one forced: the automatic choice is the staged one here)."""
     torch = torch_cuda()
     nx, ny, nz, R = 2048, 1024, 1030, 4
     if torch.cuda.get_device_properties(0).total_memory < 40 * 2 ** 30:
@@ -323,19 +324,23 @@ def test_grid_beyond_2pow31_points():
     c = synth.laplacian8_coeffs()
     u = synth.uniform_field(nx, ny, nz, seed=99)
     plan = StencilPlan(nx, ny, nz, R, c)
+    assert plan.sweep_path == "staged"
     a = torch.from_numpy(u.ravel()).cuda()
-    b = torch.full_like(a, 5.0)
-    plan.apply(a, b)
-    plan.status(None, b)
     idx = sample_interior(u.shape, R, 200000, seed=3)
     top = (nz - R - 1) * nx * ny + (ny - R - 1) * nx + np.arange(R, nx - R, dtype=np.int64)  # last interior row
     idx = np.unique(np.concatenate([idx, top]))
     assert idx.max() > 2 ** 31
-    got = b[torch.from_numpy(idx).cuda()].cpu().numpy()
     want = oracle.apply_points(u, c.astype(np.float32), R, idx)
-    assert np.max(np.abs(got.astype(np.float64) - want)) <= sweep_tol(c, u)
-    last = b[(nz - 1) * nx * ny:].cpu().numpy()
-    assert np.all(last == 5.0)  # the shell's last plane is untouched
+    for path in ("staged", "direct"):
+        plan.set_sweep_path(path)
+        b = torch.full_like(a, 5.0)
+        plan.apply(a, b)
+        plan.status(None, b)
+        got = b[torch.from_numpy(idx).cuda()].cpu().numpy()
+        assert np.max(np.abs(got.astype(np.float64) - want)) <= sweep_tol(c, u), path
+        last = b[(nz - 1) * nx * ny:].cpu().numpy()
+        assert np.all(last == 5.0), path  # the shell's last plane is untouched
+        del b
     plan.close()
 
 
