@@ -26,7 +26,7 @@ struct KernelDesc {
 };
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool NOETA = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
+          bool NOETA = false, bool SEMI = false, bool DRIFT = false, int TSTORE = 0>
 cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
                         const CUtensorMap& uprev, const CUtensorMap& v2dt2, const CUtensorMap& eta,
                         const CUtensorMap& out, const StarParams& p) {
@@ -37,7 +37,7 @@ cudaError_t launch_star(dim3 grid, cudaStream_t stream, const CUtensorMap& u,
 }
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB = 1,
-          bool NOETA = false, bool SEMI = false, bool DRIFT = false, bool TSTORE = false>
+          bool NOETA = false, bool SEMI = false, bool DRIFT = false, int TSTORE = 0>
 KernelDesc make_desc() {
   using C = StarCfg<R, TYT, NWY, STAGES, ASTAGES, WAVE, SEMI, TSTORE, KB>;
   return KernelDesc{
@@ -48,7 +48,7 @@ KernelDesc make_desc() {
       STAGES,
       C::BW,
       C::BH,
-      TSTORE,
+      TSTORE != 0,
       &launch_star<R, TYT, NWY, STAGES, ASTAGES, WAVE, MINB, KB, NOETA, SEMI, DRIFT, TSTORE>};
 }
 
@@ -69,11 +69,12 @@ KernelDesc make_desc2() {
                     C::BW, C::BH, false, &launch_star2<STAGES, MINB>};
 }
 
-// Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  `noeta`: the wave step
+// Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  The sweep's
+// configuration also depends on the grid's x-y plane (radius 4).  `noeta`: the wave step
 // of a region where eta is zero (no eta staged, no divide; the inner region of
 // wave_step_pml).  `semi`: the sweep with
 // the z stencil split into halves (stencil_apply_semi).
-KernelDesc apply_kernel_desc(int radius);
+KernelDesc apply_kernel_desc(int radius, int64_t nx, int64_t ny);  // tile shape by plane size
 // Two sweeps in one pass: built for radius 1 (fn is null for other radii).
 KernelDesc apply2_kernel_desc(int radius);
 KernelDesc semi_kernel_desc(int radius);

@@ -1,20 +1,35 @@
-// Stencil-sweep kernel instantiations, radius 1..4.
-// Tile 64 x 32 outputs, 256 threads (4 x 2 outputs per thread).  Only the lead plane is
-// read from shared memory, so the ring is the landed plane plus R+3 in flight (radius 4:
-// a 5-slot ring and one CTA barrier per 2 planes, 1-3 % faster than a barrier per plane on
-// eight of nine grid shapes from 384^3 to 2048 x 512 x 512; 7 or 8 slots are slower).
-// Radii 1-3 release ring slots warp by warp (DRIFT; at 512^3 2-6 % faster than a CTA
-// barrier per plane), radius 4 keeps the barrier (1-2 % faster there).
+// Stencil-sweep kernel instantiations, radius 1..4.  Only the lead plane is read from
+// shared memory, so the ring holds the landed plane plus the planes in flight.
+//
+// Radii 1-3: 64 x 32 tiles, 256 threads (4 x 2 outputs per thread); ring slots released
+// warp by warp (DRIFT; at 512^3 2-6 % faster than a CTA barrier per plane).
+//
+// Radius 4: 128 threads per CTA, three CTAs per SM, output tiles stored by TMA; a thread
+// owns 4 x TYT outputs, so each of its shared-memory loads of a row feeds more outputs
+// (TYT = 4: 20 float4 loads per 16 outputs and plane, against 14 per 8 with TYT = 2) at
+// 155-166 registers.  Two shapes, chosen by the size of an x-y plane (GB300, against the
+// former 64 x 32 tile of 4 x 2 outputs on 256 threads, two CTAs per SM):
+//  * planes below 2^20 points: 64 x 32 tiles of 4 x 4 per thread, a 4-slot ring, a CTA
+//    barrier per plane: 512^3 0.186 against 0.201 ms, 384^3 -6 %, 640^3 -4 %,
+//    768 x 768 x 384 -6 %, 1536 x 512 x 512 -8 %, 136 x 1000 x 200 -14 %;
+//  * larger planes: 64 x 24 tiles of 4 x 3 per thread, a 5-slot ring, a barrier per two
+//    planes: 1536 x 1536 x 256 0.834 against 0.887 ms, 2048 x 512 x 512 -9 %, 1024^3 -1 %,
+//    1152 x 1152 x 256 -11 %.  (The first shape on these grids measured 11-24 % slower
+//    than the old tile, whatever the z-chunk count or store staging depth.)
 #include "kernel_table.h"
 
 namespace libstencil {
 
-KernelDesc apply_kernel_desc(int radius) {
+constexpr int64_t kWidePlanePoints = int64_t(1) << 20;
+
+KernelDesc apply_kernel_desc(int radius, int64_t nx, int64_t ny) {
   switch (radius) {
     case 1: return make_desc<1, 2, 16, 5, 1, false, 1, 1, false, false, true>();
     case 2: return make_desc<2, 2, 16, 6, 1, false, 1, 1, false, false, true>();
     case 3: return make_desc<3, 2, 16, 7, 1, false, 1, 1, false, false, true>();
-    default: return make_desc<4, 2, 16, 5, 1, false, 2, 2, false, false, false, true>();
+    default:
+      if (nx * ny < kWidePlanePoints) return make_desc<4, 4, 8, 4, 1, false, 3, 1, false, false, false, 2>();
+      return make_desc<4, 3, 8, 5, 1, false, 3, 2, false, false, false, 2>();
   }
 }
 

@@ -698,7 +698,7 @@ stencil_plan* stencil_plan_create(int64_t nx, int64_t ny, int64_t nz, int radius
     stencil_plan_destroy(p);
     return nullptr;
   }
-  p->kd[0] = apply_kernel_desc(radius);
+  p->kd[0] = apply_kernel_desc(radius, nx, ny);
   p->kd[1] = wave_kernel_desc(radius, false);
   p->kd[2] = wave_kernel_desc(radius, true);
   p->kd[3] = semi_kernel_desc(radius);
@@ -1004,7 +1004,7 @@ int stencil_schedule_query(int64_t nx, int64_t ny, int64_t nz, int radius, int k
       nx * ny > ((int64_t)1 << 40) || nx * ny * nz > ((int64_t)1 << 40))
     return fail(STENCIL_ERR_ARG, "grid %lld x %lld x %lld out of range", (long long)nx,
                 (long long)ny, (long long)nz);
-  const KernelDesc kd = kind == 0   ? apply_kernel_desc(radius)
+  const KernelDesc kd = kind == 0   ? apply_kernel_desc(radius, nx, ny)
                         : kind == 3 ? semi_kernel_desc(radius)
                         : kind == 4 ? apply2_kernel_desc(radius)
                                     : wave_kernel_desc(radius, kind == 2);
@@ -1092,7 +1092,7 @@ extern "C" int stencil_apply_noalloc(int64_t nx, int64_t ny, int64_t nz, int rad
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   int rc = noalloc_scratch(&pl.d_status);
   if (rc) return rc;
-  pl.kd[0] = apply_kernel_desc(radius);
+  pl.kd[0] = apply_kernel_desc(radius, nx, ny);
   e = cudaFuncSetAttribute(pl.kd[0].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.kd[0].smem);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pl.occupancy[0], pl.kd[0].fn,

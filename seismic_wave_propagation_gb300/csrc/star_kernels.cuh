@@ -83,7 +83,7 @@ struct Cursor {
 };
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, bool SEMI = false,
-          bool TSTORE = false, int KB = 1>
+          int TSTORE = 0, int KB = 1>
 struct StarCfg {
   static constexpr int kThreads = kThreadsX * NWY;
   static constexpr int TY = TYT * NWY;  // output tile height
@@ -101,7 +101,9 @@ struct StarCfg {
   static constexpr int kAuxOffset = kRingOffset + STAGES * kPlaneStride;
   static constexpr int kStgOffset = kAuxOffset + (WAVE ? ASTAGES * kAuxStageBytes : 0);
   static constexpr int kStgPlaneBytes = kTX * TY * 4;  // one output tile, staged for a TMA store
-  static constexpr int kStgPlanes = TSTORE ? 2 * KB : 0;
+  // TSTORE > 0: output tiles go out by TMA store from TSTORE * KB staging tiles, so that
+  // the stores of the last TSTORE - 1 barrier intervals may still be reading theirs.
+  static constexpr int kStgPlanes = TSTORE * KB;
   static constexpr int kSmemBytes = kStgOffset + kStgPlanes * kStgPlaneBytes;
   static constexpr int XO = TSTORE ? R : 0;  // x of the first tile's first output
   static constexpr int KEEP = (WAVE || SEMI) ? R : 0;   // planes kept behind the lead
@@ -113,6 +115,7 @@ struct StarCfg {
   // TMA-stored tiles start at the interior origin x = R; the staged input box then starts
   // at x = R - kHX, which must be 0 for its x coordinate to stay 16-byte aligned.
   static_assert(!TSTORE || R == kHX, "TMA stores of the output need R == 4");
+  static_assert(TSTORE == 0 || TSTORE >= 2, "TMA stores stage at least two barrier intervals");
 };
 
 // ---- PTX wrappers ------------------------------------------------------------------
@@ -193,9 +196,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// The issuing thread's bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// All but the issuing thread's N most recent bulk-store groups have finished reading
+// shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 // The issuing thread's bulk stores are complete.
@@ -278,7 +283,7 @@ __device__ __forceinline__ void cursor_advance(const StarParams& p, Cursor& k) {
 // ---- the kernel ----------------------------------------------------------------------
 
 template <int R, int TYT, int NWY, int STAGES, int ASTAGES, bool WAVE, int MINB, int KB, bool NOETA,
-          bool SEMI, bool DRIFT, bool TSTORE>
+          bool SEMI, bool DRIFT, int TSTORE>
 __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
     star_sweep_kernel(const __grid_constant__ CUtensorMap tm_u,
                       const __grid_constant__ CUtensorMap tm_uprev,
@@ -633,9 +638,11 @@ __global__ void __launch_bounds__(kThreadsX * NWY, MINB)
       if (++since < KB && j + 1 < L) continue;
       if constexpr (TSTORE) {
         fence_proxy_async_smem();  // this thread's staged tiles become visible to the TMA unit
-        // The stores issued at the previous barrier have read their staging tiles, which
-        // the steps after this barrier may overwrite (2*KB tiles, at most KB per interval).
-        if (leader) bulk_wait_read_all();
+        // The steps after this barrier stage at most KB tiles, into the slots of the group
+        // issued TSTORE - 1 barriers before this one: all older groups must have read
+        // theirs.  Still pending then: this barrier's group and the TSTORE - 2 before it,
+        // at most (TSTORE - 1) * KB tiles right before the ones to be written.
+        if (leader) bulk_wait_read<TSTORE - 2>();
       }
       const bool stop = __syncthreads_or(failed) != 0;
       if constexpr (TSTORE) {
