@@ -590,12 +590,13 @@ void plan_regions_for(stencil_plan* p, int64_t pml) {
   // Both launches are planned on all CTA slots and run side by side; the band's items
   // take the slots the inner launch leaves or frees.  (Dividing the slots between them in
   // proportion to their work, or running the band after the inner region, measured slower.)
-  // Split only where the inner region holds at least 3/4 of the work: its points cost 0.93
-  // of the band's (640^3: 0.744 ms for a step with no eta anywhere, 0.80 ms with eta), and
-  // a thicker band of 64-wide tiles costs more in packing than that saves (640^3, 16-point
-  // band: inner share 0.71, split 1.6 % slower; 1024^3: 0.83, 13 % faster).
+  // Split only where the inner region holds at least 0.6 of the work: its points cost 0.84
+  // of the band's (640^3: 0.654 ms for a step with no eta anywhere, 0.78 ms with eta), and
+  // a thicker band of 64-wide tiles costs more in packing than that saves.  Measured on
+  // GB300 (16-point band unless noted), split against one launch: 640^3 (inner share 0.71)
+  // -6 %, 640^3 with a 32-point band (0.64) -3 %, 512^3 (0.65) -2 %, 384^3 (0.55) +8 %.
   const double all = (double)ntx * nty * (zall1 - zall0);
-  if ((double)inner.ntx * inner.nty * inner.nzi < 0.75 * all) return;
+  if ((double)inner.ntx * inner.nty * inner.nzi < 0.6 * all) return;
   const int64_t slots = (int64_t)p->num_sms * std::max(1, std::min(p->occupancy[1], p->occupancy[2]));
   geometry_regions(p, 2, &inner, 1, slots, p->reg_inner, p->reg_inner_grid);
   p->reg_band_grid = 0;

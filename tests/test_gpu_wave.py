@@ -316,7 +316,7 @@ def test_region_split_step_loop_matches_oracle(pml, dims):
     """Grids where wave_step_pml runs as two launches (inner region without eta beside the
     band with the full update): 6 steps through wave_steps in one CUDA graph, against the
     oracle's steps on the same fields."""
-    assert inner_share(dims, pml) >= 0.75  # the split path, not the single launch
+    assert inner_share(dims, pml) >= 0.6  # the split path, not the single launch
     torch = torch_cuda()
     nx, ny, nz = dims
     c = synth.laplacian8_coeffs()
