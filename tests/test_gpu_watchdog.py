@@ -17,12 +17,15 @@ from gpu_util import interior_mask, sweep_tol, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kind,R", [("apply", 4), ("apply", 1), ("semi", 4), ("wave", 4)])
-def test_lost_load_times_out_and_plan_recovers(kind, R):
-    """R = 4 sweeps close each plane with a CTA barrier, R = 1 sweeps release ring slots
-    warp by warp: both protocols must turn a lost load into a timeout."""
+@pytest.mark.parametrize("kind,R,dims", [("apply", 4, (136, 75, 41)), ("apply", 4, (1032, 1020, 14)),
+                                         ("apply", 1, (136, 75, 41)), ("semi", 4, (136, 75, 41)),
+                                         ("wave", 4, (136, 75, 41))])
+def test_lost_load_times_out_and_plan_recovers(kind, R, dims):
+    """R = 4 sweeps meet at a CTA barrier every plane (small planes) or every two planes
+    (planes of 2^20 points or more), R = 1 sweeps release ring slots warp by warp: every
+    protocol must turn a lost load into a timeout."""
     torch = torch_cuda()
-    nx, ny, nz = 136, 75, 41
+    nx, ny, nz = dims
     c = synth.laplacian8_coeffs() if R == 4 else synth.laplacian2_coeffs()
     plan = StencilPlan(nx, ny, nz, R, c)
     plan.set_sweep_path("staged")  # the direct sweep has no staged loads to lose
