@@ -226,7 +226,11 @@ class StencilPlan:
 
     def set_sweep_path(self, path) -> None:
         """stencil_plan_set_sweep_path: "auto", "staged" or "direct" (or 0, 1, 2)."""
-        _check(self._lib.stencil_plan_set_sweep_path(self._p, SWEEP_PATHS.get(path, path)))
+        if isinstance(path, str):
+            if path not in SWEEP_PATHS:
+                raise ValueError(f"sweep path must be one of {sorted(SWEEP_PATHS)}, not {path!r}")
+            path = SWEEP_PATHS[path]
+        _check(self._lib.stencil_plan_set_sweep_path(self._p, int(path)))
 
     @property
     def sweep_path(self) -> str:

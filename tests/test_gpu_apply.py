@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
-from seismic_wave_propagation_gb300 import StencilPlan, synth
+from seismic_wave_propagation_gb300 import StencilError, StencilPlan, synth
 from gpu_util import Guarded, interior_mask, sample_interior, sweep_tol, torch_cuda
 
 pytestmark = pytest.mark.gpu
@@ -85,8 +85,11 @@ def test_automatic_sweep_path(dims, R, want):
     assert plan.sweep_path != want
     plan.set_sweep_path("auto")
     assert plan.sweep_path == want
-    with pytest.raises(Exception):
+    with pytest.raises(StencilError) as ei:
         plan.set_sweep_path(3)
+    assert ei.value.code == -1
+    with pytest.raises(ValueError):
+        plan.set_sweep_path("fast")
     plan.close()
 
 
