@@ -96,7 +96,7 @@ int stencil_apply(stencil_plan* plan, const float* in, float* out, void* stream)
  *                       staged one above.
  * Both compute the same sweep up to fp32 rounding order.  Radius-1 loops (stencil_sweeps,
  * stencil_apply_host with nsweeps > 1) run most sweeps as two-sweep passes
- * (stencil_apply2) on the staged path, and on the automatic path from 7 million points,
+ * (stencil_apply2) on the staged path, and on the automatic path from 8 million points,
  * where a pass beats two direct sweeps; their other sweeps run on the plan's sweep path,
  * and the direct path runs none as passes.  stencil_debug_inject affects only the staged
  * kernels.  Returns STENCIL_OK, or STENCIL_ERR_ARG for a NULL plan or a path outside

@@ -53,20 +53,20 @@ KernelDesc make_desc() {
 }
 
 // Two radius-1 sweeps in one pass (star2_kernels.cuh).
-template <int STAGES, int MINB>
+template <int STAGES, int MINB, int NR>
 cudaError_t launch_star2(dim3 grid, cudaStream_t stream, const CUtensorMap& u, const CUtensorMap& uprev,
                          const CUtensorMap& v2dt2, const CUtensorMap& eta, const CUtensorMap& out,
                          const StarParams& p) {
-  using C = Star2Cfg<STAGES>;
-  star2_sweep_kernel<STAGES, MINB><<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, out, p);
+  using C = Star2Cfg<STAGES, NR>;
+  star2_sweep_kernel<STAGES, MINB, NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(u, uprev, v2dt2, eta, out, p);
   return cudaGetLastError();
 }
 
-template <int STAGES, int MINB>
+template <int STAGES, int MINB, int NR = 2>
 KernelDesc make_desc2() {
-  using C = Star2Cfg<STAGES>;
-  return KernelDesc{(const void*)star2_sweep_kernel<STAGES, MINB>, C::kThreads, C::kSmemBytes, C::TY, STAGES,
-                    C::BW, C::BH, false, &launch_star2<STAGES, MINB>};
+  using C = Star2Cfg<STAGES, NR>;
+  return KernelDesc{(const void*)star2_sweep_kernel<STAGES, MINB, NR>, C::kThreads, C::kSmemBytes, C::TY, STAGES,
+                    C::BW, C::BH, false, &launch_star2<STAGES, MINB, NR>};
 }
 
 // Defined in kernels_apply.cu / kernels_wave.cu; radius in [1, 4].  The sweep's

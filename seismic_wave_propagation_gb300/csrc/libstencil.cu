@@ -370,9 +370,9 @@ int get_map(stencil_plan* p, const void* ptr, int box_w, int box_h, const CUtens
 // radius 4 through 144^3 (12.3 against 14.4 us), slower at 160^3.
 constexpr int64_t kDirectMaxPoints[STENCIL_MAX_RADIUS + 1] = {0, 100000000, 12000000, 5000000, 3500000};
 // Radius-1 loops on the automatic path: from this many points a two-sweep pass of the
-// staged kernel beats two direct sweeps (GB300, chained in a graph: 192^3 10.96 against
-// 10.59 us per sweep, 256^3 21.5 against 26.9).
-constexpr int64_t kPairMinPoints = 7000000;
+// staged kernel beats two direct sweeps (GB300, chained in a graph, per sweep: 192^3 10.81
+// against 10.63 us, 224^3 16.1 against 19.1, 256^3 20.9 against 27.1).
+constexpr int64_t kPairMinPoints = 8000000;
 
 bool resolve_direct(const stencil_plan* p) {
   if (p->sweep_path == STENCIL_PATH_DIRECT) return true;

@@ -36,7 +36,7 @@ def unit_coeffs(R, seed):
                                     ((256, 96, 70), 3), ((256, 256, 128), 1)])
 def test_native_sweeps_match_oracle_run_sweeps(dims, R, nsweeps, use_graph, path):
     """On the staged path and on the automatic one: the direct kernel at these sizes, and
-    at 256 x 256 x 128 (radius 1, above 7 million points) two-sweep passes with the odd
+    at 256 x 256 x 128 (radius 1, above 8 million points) two-sweep passes with the odd
     sweeps on the direct kernel."""
     torch = torch_cuda()
     nx, ny, nz = dims
