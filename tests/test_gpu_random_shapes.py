@@ -125,3 +125,36 @@ def test_random_shape_region_split_step(nx, ny, nz, R, pml):
     tol = 1e-5 * (2 + 0.2 * float(np.sum(np.abs(c)))) * 2.0
     assert np.max(np.abs(got[m] - want[m])) <= tol
     assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD)
+
+
+def two_sweep_shapes(seed: int, count: int):
+    rng = np.random.default_rng(seed)
+    return [(4 * int(rng.integers(1, 80)), int(rng.integers(1, 140)), int(rng.integers(1, 70)))
+            for _ in range(count)]
+
+
+TWO_SWEEP_SHAPES = two_sweep_shapes(2027, 16)
+
+
+@pytest.mark.parametrize("nx,ny,nz", TWO_SWEEP_SHAPES)
+def test_random_shape_two_sweep_pass(nx, ny, nz):
+    """stencil_apply2 (radius 1) on seeded shapes ragged in every axis: 30-row tiles whose
+    last row group runs past the tile, partial x tiles, short z, empty interiors; against
+    two oracle sweeps with a fixed shell, guard bands and shell sentinels kept."""
+    torch = torch_cuda()
+    u = synth.uniform_field(nx, ny, nz, seed=nx * 5 + ny * 3 + nz)
+    c = np.random.default_rng(nx + ny).uniform(-1, 1, 2)
+    c = (c / (abs(c[0]) + 6.0 * abs(c[1]))).astype(np.float32)  # max-norm gain 1
+    plan = StencilPlan(nx, ny, nz, 1, c)
+    gin = Guarded(torch, u)
+    gout = Guarded(torch, u, fill_sentinel=True)
+    plan.apply2(gin.ptr, gout.ptr)
+    plan.status()
+    got = gout.numpy()
+    assert gin.guards_intact() and gout.guards_intact()
+    plan.close()
+    want = oracle.run_sweeps(u, c, 1, 2)
+    m = interior_mask(u.shape, 1)
+    if m.any():
+        assert np.max(np.abs(got[m].astype(np.float64) - want[m])) <= 2e-5 * float(np.max(np.abs(u)))
+    assert np.all(got.view(np.uint32)[~m] == 0x7FC0DEAD), "shell written"
