@@ -422,17 +422,19 @@ def run_ours(args, dist, rank, local, world):
 
 def run_profile_case(kind: str):
     """Three launches of the 512^3 case of one kernel (the 64^3 smoothing sweep for
-    "direct64", on the direct-load kernel): the driver for ncu captures."""
+    "direct64", on the direct-load kernel; the 25-point sweep of a 1152 x 1152 x 256 grid,
+    whose planes take the 64 x 24 tile, for "sweep_wide"): the driver for ncu captures."""
     import torch
     from seismic_wave_propagation_gb300 import StencilPlan
     n = 64 if kind == "direct64" else NX
+    dims = (1152, 1152, 256) if kind == "sweep_wide" else (n, n, n)
     r = 1 if kind in ("sweep7", "sweep7x2", "direct64") else R
     c = synth.average7_coeffs() if kind == "direct64" else synth.laplacian2_coeffs() if r == 1 else synth.laplacian8_coeffs()
-    plan = StencilPlan(n, n, n, r, c)
+    plan = StencilPlan(*dims, r, c)
     if kind == "direct64":
         plan.set_sweep_path("direct")
-    if kind in ("sweep", "semi", "sweep7", "sweep7x2", "direct64"):
-        u = torch.from_numpy(synth.uniform_field(n, n, n).ravel()).cuda()
+    if kind in ("sweep", "semi", "sweep7", "sweep7x2", "direct64", "sweep_wide"):
+        u = torch.from_numpy(synth.uniform_field(*dims).ravel()).cuda()
         o = u.clone()
         fn = {"semi": plan.apply_semi, "sweep7x2": plan.apply2}.get(kind, plan.apply)
         for _ in range(3):
@@ -447,8 +449,9 @@ def run_profile_case(kind: str):
                 plan.wave_step(f[0], f[1], nxt, f[2], f[3])
     torch.cuda.synchronize()
     plan.status()
-    k = {"sweep": 0, "sweep7": 0, "direct64": 0, "wave": 1, "wave_inner": 2, "semi": 3, "sweep7x2": 4}[kind]
-    print(json.dumps({"profile_case": kind, "grid": n, "launch": plan.launch_info(k)}))
+    k = {"sweep": 0, "sweep7": 0, "direct64": 0, "sweep_wide": 0, "wave": 1, "wave_inner": 2, "semi": 3,
+         "sweep7x2": 4}[kind]
+    print(json.dumps({"profile_case": kind, "grid": list(dims), "launch": plan.launch_info(k)}))
 
 
 def _time_loop(fn, steps, warmup, stream, warm_seconds=0.3):
@@ -687,10 +690,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-wave", action="store_true")
-    ap.add_argument("--profile", choices=["sweep", "sweep7", "sweep7x2", "wave", "wave_inner", "semi", "direct64"],
+    ap.add_argument("--profile", choices=["sweep", "sweep7", "sweep7x2", "wave", "wave_inner", "semi", "direct64",
+                                          "sweep_wide"],
                     help="run 3 launches of the 512^3 case (ncu driver); sweep7 is the 7-point Laplacian, "
                          "sweep7x2 its two-sweep pass, wave_inner the band step with no band (no-eta kernel), "
-                         "direct64 the 64^3 smoothing sweep on the direct-load kernel")
+                         "direct64 the 64^3 smoothing sweep on the direct-load kernel, sweep_wide the 25-point "
+                         "sweep of 1152 x 1152 x 256 (64 x 24 tiles)")
     ap.add_argument("--report-configs", action="store_true", help="time all five workloads")
     args = ap.parse_args()
     if args.profile or args.report_configs:
