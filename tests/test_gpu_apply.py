@@ -45,8 +45,9 @@ CASES = [
     (136, 75, 41, 1), (136, 75, 41, 2), (136, 75, 41, 3), (136, 75, 41, 4),
     (64, 64, 64, 4), (200, 33, 17, 4), (12, 12, 12, 4), (12, 9, 9, 4), (4, 5, 6, 1),
     (8, 40, 7, 2), (20, 21, 11, 3), (256, 96, 200, 4), (68, 130, 30, 1),
-    # a plane of 2^20 points or more: the radius-4 sweep's 64 x 24 tiles, ragged in x and y
-    (1100, 1000, 19, 4),
+    # planes of 2^20 points or more: the radius-4 sweep's 64 x 24 tiles, ragged in x and y;
+    # one narrow tile column 4167 tiles tall; a plane just past 2^20 points
+    (1100, 1000, 19, 4), (12, 100000, 10, 4), (2052, 520, 13, 4),
 ]
 
 
