@@ -344,3 +344,33 @@ def test_region_split_step_loop_matches_oracle(pml, dims):
     m = interior_mask(u.shape, 4)
     np.testing.assert_array_equal(got[~m], b[~m])
     plan.close()
+
+
+def test_wave_step_beyond_2pow31_points():
+    """64-bit indexing of the fused wave step: 2048 x 1024 x 1030 = 2.16e9 points (8.6 GB
+    per field), sampled against the oracle, including the last interior row.  u_prev and u
+    are one field and v2dt2 and eta another (allowed: only u_next must not overlap them)."""
+    torch = torch_cuda()
+    nx, ny, nz, R = 2048, 1024, 1030, 4
+    if torch.cuda.get_device_properties(0).total_memory < 60 * 2 ** 30:
+        pytest.skip("needs ~30 GB of device memory")
+    c = synth.laplacian8_coeffs()
+    c32 = c.astype(np.float32)
+    u = synth.uniform_field(nx, ny, nz, seed=98)
+    s = (np.abs(u) * np.float32(0.05)).astype(np.float32)  # v2dt2 and eta in [0, 0.05]
+    plan = StencilPlan(nx, ny, nz, R, c)
+    du = torch.from_numpy(u.ravel()).cuda()
+    ds = torch.from_numpy(s.ravel()).cuda()
+    dn = torch.full_like(du, 5.0)
+    plan.wave_step(du, du, dn, ds, ds)
+    plan.status(None, dn)
+    idx = sample_interior(u.shape, R, 200000, seed=4)
+    top = (nz - R - 1) * nx * ny + (ny - R - 1) * nx + np.arange(R, nx - R, dtype=np.int64)  # last interior row
+    idx = np.unique(np.concatenate([idx, top]))
+    assert idx.max() > 2 ** 31
+    got = dn[torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.float64)
+    want = oracle.wave_points(u, u, s, s, c32, R, idx)
+    tol = 1e-5 * (3 + 0.05 * float(np.sum(np.abs(c32)))) * float(np.max(np.abs(u))) * 2.0
+    assert np.max(np.abs(got - want)) <= tol
+    assert np.all(dn[(nz - 1) * nx * ny:].cpu().numpy() == 5.0)  # the shell's last plane is untouched
+    plan.close()
