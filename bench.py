@@ -594,8 +594,11 @@ def run_report_configs(args):
                 bufs = [a, a.clone()]
                 nsw = w["sweeps"]
 
-                def loop():  # the workload's ping-pong sweeps, one graph launch
-                    plan.sweeps(bufs[0], bufs[1], nsw, True, stream)
+                def loop():  # the workload's ping-pong sweeps, one graph launch (one sweep: one launch)
+                    if nsw == 1:
+                        plan.apply(bufs[0], bufs[1], stream)
+                    else:
+                        plan.sweeps(bufs[0], bufs[1], nsw, True, stream)
                 units, per = nsw, traffic.apply_bytes(nx, ny, nz, r)
             reps = max(1, min(101, int(2000 // max(1, units))))
             ms = _time_loop(loop, reps, 3, stream)
